@@ -1,0 +1,17 @@
+"""Fixed-order, batch-invariant row softmax for GB300 (sm_103a).
+
+The operation between the QK and AV GEMMs of joint attention ("[WS1][kernels] Add fixed-order
+joint-attention softmax for Qwen-Image", Summary): forward P and LSE with optional causal /
+valid-length / key masks and a per-head sink logit; backward delta and dScores; the per-head
+sink gradient without atomics.  The compute lives in ``libfos_softmax.so`` (C ABI in
+``include/fos_softmax.h``); this package is its PyTorch binding.
+"""
+
+from ._build import build
+from .binding import (FosError, Launch, fos_contract_fingerprint, fos_device_error,
+                      fos_sink_grad, fos_softmax_bwd, fos_softmax_fwd, fos_status_string)
+
+__all__ = [
+    "FosError", "Launch", "build", "fos_contract_fingerprint", "fos_device_error",
+    "fos_sink_grad", "fos_softmax_bwd", "fos_softmax_fwd", "fos_status_string",
+]

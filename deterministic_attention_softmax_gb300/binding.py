@@ -1,0 +1,232 @@
+"""PyTorch-facing binding of the C ABI, with the same names as ``include/fos_softmax.h``.
+
+Argument marshalling only: tensors are checked for device, dtype and layout, their device
+pointers and the current CUDA stream are passed to ``libfos_softmax.so``, and a non-OK status
+becomes a ``FosError``.  PyTorch provides device memory and streams; all arithmetic happens in
+the library's CUDA kernels.
+
+Row layout: ``scores`` (and P, dP, dScores) is a tensor whose last dimension holds the keys
+(stride 1) and whose leading dimensions collapse to rows with one uniform row stride ``ld``
+(``ld >= key_len``): a 2-D ``[rows, key_len]`` tensor, a narrowed view of a wider buffer, or a
+``[batch, heads, q_len, key_len]`` tensor.  Rows are ordered ``[batch][heads][q_len]``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _abi
+
+_DTYPES = {torch.float32: _abi.FOS_F32, torch.bfloat16: _abi.FOS_BF16,
+           torch.float16: _abi.FOS_F16}
+
+
+class FosError(RuntimeError):
+    """A non-OK ``fos_status``; ``.status`` holds the code."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        msg = _abi.lib().fos_status_string(self.status).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+@dataclass
+class Launch:
+    """Optional launch geometry (none of it changes a result bit); 0 means the default."""
+
+    warps_per_cta: int = 0
+    ctas: int = 0
+    stages: int = 0
+    load_path: int = 0  # 0 auto, 1 bulk copy (TMA) only, 2 plain loads only
+    wait_timeout_ns: int = 0
+    test_stall: int = 0
+
+    def _c(self) -> _abi.FosLaunch:
+        return _abi.FosLaunch(self.warps_per_cta, self.ctas, self.stages, self.load_path,
+                              self.wait_timeout_ns, self.test_stall, 0)
+
+
+def _rows_layout(t: torch.Tensor, name: str):
+    """(rows, key_len, ld) of a row-major key tensor, or raise."""
+    if t.dim() < 2:
+        raise ValueError(f"{name} must have at least 2 dimensions (rows x keys)")
+    if t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"{name}: the key dimension must have stride 1")
+    L = t.shape[-1]
+    ld = t.stride(-2) if t.shape[-2] > 1 else max(L, t.stride(-2))
+    rows = 1
+    for d in t.shape[:-1]:
+        rows *= d
+    expect = ld
+    for i in range(t.dim() - 2, -1, -1):
+        if t.shape[i] > 1 and t.stride(i) != expect:
+            raise ValueError(f"{name}: leading dimensions do not collapse to one row stride")
+        expect *= t.shape[i]
+    return rows, L, ld
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(t, name, device):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _geometry(x, batch, heads, q_len):
+    rows, L, ld = _rows_layout(x, "scores")
+    if x.dim() == 4 and batch is None and heads is None and q_len is None:
+        batch, heads, q_len = x.shape[0], x.shape[1], x.shape[2]
+    batch = 1 if batch is None else int(batch)
+    heads = 1 if heads is None else int(heads)
+    if q_len is None:
+        q_len = rows // max(1, batch * heads)
+    return rows, L, ld, batch, heads, int(q_len)
+
+
+def _desc(rows, L, ld, batch, heads, q_len, causal, kv_valid_len, key_mask, sink):
+    if kv_valid_len is not None and (kv_valid_len.dtype != torch.int32 or
+                                     not kv_valid_len.is_contiguous()):
+        raise ValueError("kv_valid_len must be a contiguous int32 tensor [batch]")
+    if key_mask is not None:
+        if key_mask.dtype not in (torch.uint8, torch.bool) or not key_mask.is_contiguous():
+            raise ValueError("key_mask must be a contiguous uint8/bool tensor [batch, key_len]")
+        if key_mask.numel() != batch * L:
+            raise ValueError("key_mask must have batch * key_len entries")
+    if sink is not None:
+        if sink.dtype != torch.float32 or not sink.is_contiguous() or sink.numel() != heads:
+            raise ValueError("sink must be a contiguous float32 tensor [heads]")
+    if kv_valid_len is not None and kv_valid_len.numel() != batch:
+        raise ValueError("kv_valid_len must have one entry per batch")
+    return _abi.FosDesc(rows, ld, L, batch, heads, q_len, int(bool(causal)), 0,
+                        None if kv_valid_len is None else kv_valid_len.data_ptr(),
+                        None if key_mask is None else key_mask.data_ptr(),
+                        None if sink is None else sink.data_ptr())
+
+
+def _like(x):
+    return torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+
+
+def _same_layout(a, b, na, nb):
+    if a.shape != b.shape or a.stride() != b.stride() or a.dtype != b.dtype:
+        raise ValueError(f"{nb} must have the shape, strides and dtype of {na}")
+
+
+def fos_softmax_fwd(scores, probs=None, lse=None, *, batch=None, heads=None, q_len=None,
+                    causal=False, kv_valid_len=None, key_mask=None, sink=None, stream=None,
+                    launch: Launch | None = None):
+    """Fixed-order softmax forward.  Returns ``(probs, lse)``; see ``fos_softmax_fwd`` in the
+    C header for the arithmetic.  ``probs`` may be ``scores`` itself (in place)."""
+    if scores.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {scores.dtype}")
+    dev = scores.device
+    rows, L, ld, batch, heads, q_len = _geometry(scores, batch, heads, q_len)
+    if probs is None:
+        probs = _like(scores)
+    if lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    _same_layout(scores, probs, "scores", "probs")
+    if lse.dtype != torch.float32 or lse.numel() != rows or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor with one entry per row")
+    for t, n in ((scores, "scores"), (probs, "probs"), (lse, "lse"), (kv_valid_len, "kv_valid_len"),
+                 (key_mask, "key_mask"), (sink, "sink")):
+        _check_cuda(t, n, dev)
+    d = _desc(rows, L, ld, batch, heads, q_len, causal, kv_valid_len, key_mask, sink)
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_softmax_fwd(ctypes.byref(d), _DTYPES[scores.dtype], _ptr(scores),
+                                        _ptr(probs), _ptr(lse), _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_softmax_fwd")
+    return probs, lse
+
+
+def fos_softmax_bwd(probs, dprobs, dscores=None, delta=None, *, batch=None, heads=None,
+                    q_len=None, causal=False, kv_valid_len=None, key_mask=None, stream=None,
+                    want_delta=True, launch: Launch | None = None):
+    """Softmax VJP on the given P.  Returns ``(dscores, delta)`` (delta is None when neither
+    given nor wanted).  ``dscores`` may be ``dprobs`` itself (in place)."""
+    if probs.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {probs.dtype}")
+    dev = probs.device
+    rows, L, ld, batch, heads, q_len = _geometry(probs, batch, heads, q_len)
+    _same_layout(probs, dprobs, "probs", "dprobs")
+    if dscores is None:
+        dscores = _like(probs)
+    _same_layout(probs, dscores, "probs", "dscores")
+    if delta is None and want_delta:
+        delta = torch.empty(rows, dtype=torch.float32, device=dev)
+    if delta is not None and (delta.dtype != torch.float32 or delta.numel() != rows or
+                              not delta.is_contiguous()):
+        raise ValueError("delta must be a contiguous float32 tensor with one entry per row")
+    for t, n in ((probs, "probs"), (dprobs, "dprobs"), (dscores, "dscores"), (delta, "delta"),
+                 (kv_valid_len, "kv_valid_len"), (key_mask, "key_mask")):
+        _check_cuda(t, n, dev)
+    d = _desc(rows, L, ld, batch, heads, q_len, causal, kv_valid_len, key_mask, None)
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_softmax_bwd(ctypes.byref(d), _DTYPES[probs.dtype], _ptr(probs),
+                                        _ptr(dprobs), _ptr(dscores), _ptr(delta),
+                                        _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_softmax_bwd")
+    return dscores, delta
+
+
+def fos_sink_grad(lse, delta, sink, d_sink=None, *, batch, heads, q_len, key_len=1,
+                  stream=None, launch: Launch | None = None):
+    """Per-head sink gradient from the forward's LSE and the backward's delta."""
+    dev = lse.device
+    rows = int(batch) * int(heads) * int(q_len)
+    for t, n in ((lse, "lse"), (delta, "delta")):
+        if t.dtype != torch.float32 or t.numel() != rows or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 tensor of batch*heads*q_len")
+    if d_sink is None:
+        d_sink = torch.empty(int(heads), dtype=torch.float32, device=dev)
+    if d_sink.dtype != torch.float32 or d_sink.numel() != heads or not d_sink.is_contiguous():
+        raise ValueError("d_sink must be a contiguous float32 tensor [heads]")
+    for t, n in ((lse, "lse"), (delta, "delta"), (sink, "sink"), (d_sink, "d_sink")):
+        _check_cuda(t, n, dev)
+    if sink is None:
+        raise ValueError("sink is required")
+    L = max(1, int(key_len))
+    d = _desc(rows, L, L, int(batch), int(heads), int(q_len), False, None, None, sink)
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_sink_grad(ctypes.byref(d), _ptr(lse), _ptr(delta), _ptr(d_sink),
+                                      _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_sink_grad")
+    return d_sink
+
+
+def fos_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return int(_abi.lib().fos_device_error(_stream_handle(stream, dev)))
+
+
+def fos_status_string(status: int) -> str:
+    return _abi.lib().fos_status_string(int(status)).decode()
+
+
+def fos_contract_fingerprint() -> str:
+    return _abi.lib().fos_contract_fingerprint().decode()

@@ -1,0 +1,299 @@
+// fos_api.cu -- the C ABI of libfos_softmax.so (declared in include/fos_softmax.h).
+//
+// Host side only: argument validation, the choice of load path and launch geometry, the
+// per-device set-up (SM count, shared-memory limit, kernel attributes, the address of the
+// device error word) and the status strings.  None of these choices changes a result bit.
+#include <limits.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fos_internal.h"
+
+namespace fos {
+
+// Device error word: a kernel whose bounded wait ran out stores kDevErrTimeout here.
+__device__ unsigned g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kBarBytes = 128;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kDefaultWarps = 8;
+constexpr size_t kStageTarget = 64 * 1024;  // ring bytes per CTA aimed at by default
+constexpr int kMaxStages = 16;
+
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  int max_smem = 0;  // opt-in dynamic shared memory per block
+  unsigned *err = nullptr;
+};
+
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+fos_status device_info(DevInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FOS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FOS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return FOS_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return FOS_ERR_CUDA;
+    d.err = static_cast<unsigned *>(p);
+    const fos_dtype dts[3] = {FOS_F32, FOS_BF16, FOS_F16};
+    for (fos_dtype dt : dts) {
+      if (fwd_prepare(dt, d.max_smem) != cudaSuccess) return FOS_ERR_CUDA;
+      if (bwd_prepare(dt, d.max_smem) != cudaSuccess) return FOS_ERR_CUDA;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return FOS_OK;
+}
+
+int dtype_size(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return 4;
+    case FOS_BF16: return 2;
+    case FOS_F16: return 2;
+  }
+  return 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fos_status check_desc(const fos_desc *d) {
+  if (d == nullptr) return FOS_ERR_INVALID;
+  if (d->reserved != 0) return FOS_ERR_INVALID;
+  if (d->rows < 0 || d->key_len < 1 || d->ld < d->key_len) return FOS_ERR_INVALID;
+  if (d->causal != 0 && d->causal != 1) return FOS_ERR_INVALID;
+  if (d->batch < 0 || d->heads < 0 || d->q_len < 0) return FOS_ERR_INVALID;
+  const int64_t prod = (int64_t)d->batch * d->heads * d->q_len;
+  if (prod != d->rows) return FOS_ERR_INVALID;
+  if (d->causal && d->q_len > d->key_len) return FOS_ERR_INVALID;
+  // rows * ld * 4 bytes must stay addressable
+  if (d->rows > 0 && d->ld > (INT64_MAX / 8) / d->rows) return FOS_ERR_INVALID;
+  return FOS_OK;
+}
+
+fos_status check_launch(const fos_launch *l) {
+  if (l == nullptr) return FOS_OK;
+  if (l->warps_per_cta < 0 || l->warps_per_cta > 16) return FOS_ERR_INVALID;
+  if (l->ctas < 0) return FOS_ERR_INVALID;
+  if (l->stages < 0 || l->stages > kMaxStages) return FOS_ERR_INVALID;
+  if (l->load_path < 0 || l->load_path > 2) return FOS_ERR_INVALID;
+  if (l->wait_timeout_ns < 0) return FOS_ERR_INVALID;
+  if (l->test_stall != 0 && l->test_stall != 1) return FOS_ERR_INVALID;
+  if (l->reserved != 0) return FOS_ERR_INVALID;
+  return FOS_OK;
+}
+
+// Geometry of a row-kernel launch.
+struct Plan {
+  int threads = 0;
+  int grid = 0;
+  size_t smem = 0;
+  int stages = 1;
+  bool bulk = false;
+};
+
+// Fills the shared part of RowArgs and picks path, stages, CTAs.  `inputs` are the row
+// arrays that are staged (scores, or P and dP); `copies` is how many of them a stage holds.
+template <typename OccFn>
+fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs, int copies,
+                     const void *output, const fos_launch *l, const DevInfo &dev,
+                     size_t (*extra)(int, int), OccFn occ, RowArgs *ra, Plan *pl) {
+  const int esz = dtype_size(dt);
+  const int T = (d->key_len + kTileK - 1) / kTileK;
+  const size_t stage_bytes = (size_t)T * kTileK * esz;
+  const bool stride16 = ((d->ld * esz) & 15) == 0;
+  bool in_aligned = stride16;
+  for (int i = 0; i < copies; ++i) in_aligned = in_aligned && aligned16(inputs[i]);
+  const bool bulk_ok = in_aligned && (((int64_t)d->key_len * esz) & 15) == 0;
+  const int path = l ? l->load_path : 0;
+  if (path == 1 && !bulk_ok) return FOS_ERR_UNSUPPORTED;
+  const bool bulk = (path == 1) || (path == 0 && bulk_ok);
+
+  const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : kDefaultWarps;
+  const size_t slot = (size_t)copies * stage_bytes;
+  const size_t fixed = extra(T, 0);
+  if (fixed + slot > (size_t)dev.max_smem) return FOS_ERR_UNSUPPORTED;
+  int stages = 1;
+  if (bulk) {
+    if (l && l->stages) {
+      stages = l->stages;
+    } else {
+      stages = (int)(kStageTarget / slot);
+      stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    }
+    while (stages > 1 && fixed + stages * slot > (size_t)dev.max_smem) --stages;
+    if (l && l->stages && stages != l->stages) return FOS_ERR_UNSUPPORTED;
+  }
+  const size_t smem = fixed + stages * slot;
+
+  int grid = 0;
+  if (l && l->ctas) {
+    grid = l->ctas;
+  } else {
+    int per_sm = 0;
+    if (occ(warps * 32, smem, &per_sm) != cudaSuccess) return FOS_ERR_CUDA;
+    if (per_sm < 1) return FOS_ERR_UNSUPPORTED;
+    grid = per_sm * dev.sms;
+  }
+  if ((int64_t)grid > d->rows) grid = (int)d->rows;
+
+  ra->rows = d->rows;
+  ra->ld = d->ld;
+  ra->L = d->key_len;
+  ra->heads = d->heads;
+  ra->q_len = d->q_len;
+  ra->causal = d->causal;
+  ra->kv_valid_len = d->kv_valid_len;
+  ra->key_mask = d->key_mask;
+  ra->T = T;
+  ra->stages = stages;
+  ra->stage_bytes = (uint32_t)stage_bytes;
+  ra->use_bulk = bulk ? 1 : 0;
+  ra->in_vec = in_aligned ? 1 : 0;
+  ra->out_vec = (stride16 && aligned16(output)) ? 1 : 0;
+  ra->timeout_ns = (l && l->wait_timeout_ns) ? (uint64_t)l->wait_timeout_ns : kDefaultTimeoutNs;
+  ra->test_stall = l ? l->test_stall : 0;
+  ra->err = dev.err;
+
+  pl->threads = warps * 32;
+  pl->grid = grid;
+  pl->smem = smem;
+  pl->stages = stages;
+  pl->bulk = bulk;
+  return FOS_OK;
+}
+
+}  // namespace
+}  // namespace fos
+
+using namespace fos;
+
+extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
+                                      void *probs, float *lse, cudaStream_t stream,
+                                      const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
+  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
+  if (scores == nullptr || probs == nullptr || lse == nullptr) return FOS_ERR_INVALID;
+  DevInfo *dev = nullptr;
+  if ((st = device_info(&dev)) != FOS_OK) return st;
+
+  FwdArgs a{};
+  Plan pl;
+  const void *inputs[1] = {scores};
+  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem,
+                 [dtype](int th, size_t sm, int *n) { return fwd_occupancy(dtype, th, sm, n); },
+                 &a, &pl);
+  if (st != FOS_OK) return st;
+  a.scores = scores;
+  a.probs = probs;
+  a.lse = lse;
+  a.sink = desc->sink;
+  if (fwd_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+    return FOS_ERR_CUDA;
+  return FOS_OK;
+}
+
+extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *probs,
+                                      const void *dprobs, void *dscores, float *delta,
+                                      cudaStream_t stream, const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
+  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
+  if (probs == nullptr || dprobs == nullptr || dscores == nullptr) return FOS_ERR_INVALID;
+  DevInfo *dev = nullptr;
+  if ((st = device_info(&dev)) != FOS_OK) return st;
+
+  BwdArgs a{};
+  Plan pl;
+  const void *inputs[2] = {probs, dprobs};
+  st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
+                 [dtype](int th, size_t sm, int *n) { return bwd_occupancy(dtype, th, sm, n); },
+                 &a, &pl);
+  if (st != FOS_OK) return st;
+  a.probs = probs;
+  a.dprobs = dprobs;
+  a.dscores = dscores;
+  a.delta = delta;
+  if (bwd_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+    return FOS_ERR_CUDA;
+  return FOS_OK;
+}
+
+extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
+                                    float *d_sink, cudaStream_t stream,
+                                    const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (desc->sink == nullptr || lse == nullptr || delta == nullptr || d_sink == nullptr)
+    return FOS_ERR_INVALID;
+  if (desc->heads == 0) return FOS_OK;
+  if (desc->rows == 0) return FOS_ERR_INVALID;  // heads > 0 with no rows: nothing defines d_sink
+  DevInfo *dev = nullptr;
+  if ((st = device_info(&dev)) != FOS_OK) return st;
+  SinkArgs a{};
+  a.batch = desc->batch;
+  a.heads = desc->heads;
+  a.q_len = desc->q_len;
+  a.sink = desc->sink;
+  a.lse = lse;
+  a.delta = delta;
+  a.d_sink = d_sink;
+  const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
+  if (sink_launch(a, warps * 32, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  return FOS_OK;
+}
+
+extern "C" fos_status fos_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FOS_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return FOS_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return FOS_ERR_CUDA;
+    return FOS_ERR_TIMEOUT;
+  }
+  return FOS_OK;
+}
+
+extern "C" const char *fos_status_string(fos_status status) {
+  switch (status) {
+    case FOS_OK: return "FOS_OK";
+    case FOS_ERR_INVALID: return "FOS_ERR_INVALID: invalid argument";
+    case FOS_ERR_UNSUPPORTED: return "FOS_ERR_UNSUPPORTED: valid but not supported by the kernels";
+    case FOS_ERR_CUDA: return "FOS_ERR_CUDA: CUDA launch or runtime error";
+    case FOS_ERR_TIMEOUT: return "FOS_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+  }
+  return "unknown fos_status";
+}
+
+extern "C" const char *fos_contract_fingerprint(void) {
+  return "fos-softmax contract 1; sm_103a; TILE_K=256; lane l owns keys 8l..8l+7 of a tile, "
+         "combined in ascending order; warp xor tree 16,8,4,2,1 for max and sums; "
+         "online merge of tile states left to right from (sink,1) or (-inf,0), "
+         "S=S*exp(Mprev-M)+s_t*exp(m_t-M), exp(a-b):=1 when a==b; "
+         "exp(x)=ex2.approx.f32(rn(x*rn(log2 e))); P=rn(e_j*rn(exp(m_t-M)/S)); "
+         "LSE=M+logf(S); delta: lane fma chain, xor tree, tiles left to right; "
+         "dS=fma(P,rn(dP-delta),+0); d_sink: rows of a head in (b,i) order, chunks of 256 "
+         "with the same lane/tree layout, chunks left to right; "
+         "float32 intermediates, one rounding to the I/O dtype (RNE); no FMA contraction, "
+         "no fast-math, no atomics, no split rows, no tensor cores";
+}

@@ -1,0 +1,272 @@
+// fos_bwd.cu -- backward kernel of the fixed-order row softmax (delta, dScores), sm_103a.
+//
+// The softmax VJP on the P the caller passes in ("[WS1][kernels] Add fixed-order
+// joint-attention softmax for Qwen-Image", Summary, "Fixed-order backward"):
+//
+//   delta = fixed_sum(P * dP)          dScores_j = P_j * (dP_j - delta)
+//
+// with the forward's tile layout and order: inside tile t lane l multiplies and accumulates
+// keys 256t + 8l .. +7 in ascending order with fused multiply-adds, the lanes are combined by
+// the xor tree (16, 8, 4, 2, 1), and tile partials are added left to right.  dScores is formed
+// as fma(P_j, dP_j - delta, +0) so that a zero product is +0 whatever the sign of the
+// difference, and rounded once.  Masked keys are skipped in the sum and written as +0.
+//
+// Structure as in the forward: persistent CTAs, a ring of staged rows (P and dP of a row
+// arrive by two 1-D bulk copies on one mbarrier), one CTA per row at a time; warp 0 adds the
+// tile partials, everything else is tile-parallel over the warps.
+#include "fos_device.cuh"
+#include "fos_internal.h"
+
+namespace fos {
+namespace {
+
+constexpr int kKT = 4;          // tiles per warp whose P and dP stay in registers
+constexpr int kBarBytes = 128;  // room for up to 16 mbarriers at the start of smem
+
+__device__ __forceinline__ bool key_ok(int j, int lim, const uint8_t *km) {
+  return (j < lim) && (km == nullptr || km[j] != 0);
+}
+
+// Lane-local ascending fused multiply-add over the lane's 8 keys, then the xor tree.
+__device__ __forceinline__ float tile_dot(const float (&p)[8], const float (&d)[8], int j0, int lim,
+                                          const uint8_t *km) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kLaneKeys; ++q)
+    if (key_ok(j0 + q, lim, km)) acc = __fmaf_rn(p[q], d[q], acc);
+  return warp_sum_xor(acc);
+}
+
+__device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[8], int j0,
+                                          int lim, const uint8_t *km, float delta,
+                                          float (&v)[8]) {
+#pragma unroll
+  for (int q = 0; q < kLaneKeys; ++q)
+    v[q] = key_ok(j0 + q, lim, km) ? __fmaf_rn(p[q], __fsub_rn(d[q], delta), 0.0f) : 0.0f;
+}
+
+template <typename T>
+__device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
+                                            int lim, bool vec) {
+  constexpr int esz = Io<T>::kEsz;
+  int start = 0;
+  if (vec) {
+    const int n16 = (lim * esz) >> 4;
+    for (int c = threadIdx.x; c < n16; c += blockDim.x)
+      reinterpret_cast<uint4 *>(stage)[c] = reinterpret_cast<const uint4 *>(src)[c];
+    start = (n16 << 4) / esz;
+  }
+  for (int j = start + threadIdx.x; j < lim; j += blockDim.x) {
+    if (esz == 4)
+      reinterpret_cast<uint32_t *>(stage)[j] = reinterpret_cast<const uint32_t *>(src)[j];
+    else
+      reinterpret_cast<uint16_t *>(stage)[j] = reinterpret_cast<const uint16_t *>(src)[j];
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void issue_row(const BwdArgs &a, int64_t rr, unsigned char *stage,
+                                          uint64_t *bar) {
+  constexpr int esz = Io<T>::kEsz;
+  int b, h;
+  const int lim = row_limit(rr, a.L, a.heads, a.q_len, a.causal, a.kv_valid_len, &b, &h);
+  const uint32_t bytes = ((uint32_t)lim * esz + 15u) & ~15u;
+  const uint32_t bar_a = smem_addr(bar);
+  mbar_arrive_expect_tx(bar_a, 2u * bytes);
+  if (bytes) {
+    const size_t off = (size_t)rr * a.ld * esz;
+    bulk_g2s(smem_addr(stage), static_cast<const unsigned char *>(a.probs) + off, bytes, bar_a);
+    bulk_g2s(smem_addr(stage + a.stage_bytes), static_cast<const unsigned char *>(a.dprobs) + off,
+             bytes, bar_a);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  using Raw = typename Io<T>::Raw;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+  unsigned char *ring = smem + kBarBytes;
+  const size_t slot = 2 * (size_t)a.stage_bytes;
+  float *td = reinterpret_cast<float *>(ring + (size_t)a.stages * slot);
+  float *dsm = td + a.T;  // delta of the current row, for every warp
+
+  const int tid = threadIdx.x;
+  const int nw = blockDim.x >> 5;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t G = gridDim.x;
+  const int64_t r0 = blockIdx.x;
+  if (r0 >= a.rows) return;
+  const int64_t nmine = (a.rows - 1 - r0) / G + 1;
+  const int NS = a.stages;
+  const bool stall = a.test_stall && blockIdx.x == 0;
+  int64_t issued_end = 0;
+
+  if (a.use_bulk) {
+    if (tid == 0) {
+      for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&bars[s]), 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int64_t kk = 0; kk < nmine && kk < NS; ++kk)
+        if (!(stall && kk == 0)) issue_row<T>(a, r0 + kk * G, ring + (size_t)kk * slot, &bars[kk]);
+    }
+    issued_end = nmine < NS ? nmine : NS;
+  }
+
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * G;
+    const int s = a.use_bulk ? (int)(k % NS) : 0;
+    unsigned char *sp = ring + (size_t)s * slot;
+    unsigned char *sd = sp + a.stage_bytes;
+    int b, h;
+    const int lim = row_limit(r, a.L, a.heads, a.q_len, a.causal, a.kv_valid_len, &b, &h);
+    const int Te = (lim + kTileK - 1) / kTileK;
+    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)b * a.L : nullptr;
+    const bool in_regs = Te <= nw * kKT;
+
+    bool timed_out = false;
+    if (a.use_bulk) {
+      timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((k / NS) & 1), a.timeout_ns);
+    } else {
+      const size_t off = (size_t)r * a.ld * esz;
+      plain_stage<T>(sp, static_cast<const unsigned char *>(a.probs) + off, lim, a.in_vec != 0);
+      plain_stage<T>(sd, static_cast<const unsigned char *>(a.dprobs) + off, lim, a.in_vec != 0);
+      __syncthreads();
+    }
+
+    // ---- pass 1: tile partials of delta
+    Raw rp[kKT], rd[kKT];
+    if (in_regs) {
+#pragma unroll
+      for (int kk = 0; kk < kKT; ++kk) {
+        const int t = w + kk * nw;
+        if (t < Te) {
+          const int j0 = t * kTileK + lane * kLaneKeys;
+          rp[kk] = Io<T>::lds(sp + (size_t)j0 * esz);
+          rd[kk] = Io<T>::lds(sd + (size_t)j0 * esz);
+          float p[8], d[8];
+          Io<T>::widen(rp[kk], p);
+          Io<T>::widen(rd[kk], d);
+          const float part = tile_dot(p, d, j0, lim, km);
+          if (lane == 0) td[t] = part;
+        }
+      }
+    } else {
+      for (int t = w; t < Te; t += nw) {
+        const int j0 = t * kTileK + lane * kLaneKeys;
+        float p[8], d[8];
+        Io<T>::widen(Io<T>::lds(sp + (size_t)j0 * esz), p);
+        Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
+        const float part = tile_dot(p, d, j0, lim, km);
+        if (lane == 0) td[t] = part;
+      }
+    }
+
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) {
+        raise_device_error(a.err, kDevErrTimeout);
+        for (int64_t kk = k; kk < issued_end; ++kk) {
+          if (stall && kk == 0) continue;
+          mbar_wait_bounded(smem_addr(&bars[kk % NS]), (uint32_t)((kk / NS) & 1), a.timeout_ns);
+        }
+      }
+      return;
+    }
+
+    if (a.use_bulk && in_regs && tid == 0 && k + NS < nmine) {
+      issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s]);
+      issued_end = k + NS + 1;
+    }
+
+    // ---- tile partials added left to right (one thread)
+    if (tid == 0) {
+      float delta = 0.0f;
+      for (int t = 0; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
+      dsm[0] = delta;
+      if (a.delta) a.delta[r] = delta;
+    }
+    __syncthreads();
+    const float delta = dsm[0];
+
+    // ---- pass 2: dScores
+    unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
+    const bool ovec = a.out_vec != 0;
+    if (in_regs) {
+#pragma unroll
+      for (int kk = 0; kk < kKT; ++kk) {
+        const int t = w + kk * nw;
+        if (t < Te) {
+          const int j0 = t * kTileK + lane * kLaneKeys;
+          float p[8], d[8], v[8];
+          Io<T>::widen(rp[kk], p);
+          Io<T>::widen(rd[kk], d);
+          tile_grad(p, d, j0, lim, km, delta, v);
+          store_lane8<T>(grow, j0, a.L, ovec, v);
+        }
+      }
+    } else {
+      for (int t = w; t < Te; t += nw) {
+        const int j0 = t * kTileK + lane * kLaneKeys;
+        float p[8], d[8], v[8];
+        Io<T>::widen(Io<T>::lds(sp + (size_t)j0 * esz), p);
+        Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
+        tile_grad(p, d, j0, lim, km, delta, v);
+        store_lane8<T>(grow, j0, a.L, ovec, v);
+      }
+    }
+    for (int t = Te + w; t < a.T; t += nw) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+
+    if (!in_regs) {
+      __syncthreads();
+      if (a.use_bulk && tid == 0 && k + NS < nmine) {
+        issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s]);
+        issued_end = k + NS + 1;
+      }
+    }
+  }
+}
+
+const void *bwd_fn(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_kernel<float>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__nv_bfloat16>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__half>);
+  }
+  return nullptr;
+}
+
+}  // namespace
+
+size_t bwd_extra_smem(int T, int stages) {
+  (void)stages;
+  return (size_t)kBarBytes + (size_t)(T + 4) * sizeof(float);
+}
+
+cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {
+  return cudaFuncSetAttribute(bwd_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+cudaError_t bwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, bwd_fn(dt), threads, smem);
+}
+
+cudaError_t bwd_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                       cudaStream_t s) {
+  switch (dt) {
+    case FOS_F32: fos_bwd_kernel<float><<<grid, threads, smem, s>>>(a); break;
+    case FOS_BF16: fos_bwd_kernel<__nv_bfloat16><<<grid, threads, smem, s>>>(a); break;
+    case FOS_F16: fos_bwd_kernel<__half><<<grid, threads, smem, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fos

@@ -1,0 +1,247 @@
+// fos_device.cuh -- device-side building blocks of the fixed-order row softmax (sm_103a).
+//
+// Everything that fixes a result bit lives here, so the forward, backward and sink kernels
+// share one arithmetic contract:
+//   * exp_fos / scale_fos  -- the exponential and the guarded rescale factor;
+//   * warp_max_xor / warp_sum_xor -- the fixed xor-shuffle trees (offsets 16, 8, 4, 2, 1);
+//   * Io<T> -- widening loads of 8 keys and the single rounding to the I/O dtype.
+// The rest is data movement: mbarrier and 1-D bulk-copy (TMA) wrappers with bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fos_internal.h"
+
+#ifdef __USE_FAST_MATH__
+#error "libfos_softmax must be built without fast-math: it would change the arithmetic contract"
+#endif
+
+namespace fos {
+
+constexpr int kLaneKeys = 8;   // contiguous keys per lane inside a tile
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kDevErrTimeout = 1u;  // value stored in the device error word
+
+// ------------------------------------------------------------------ arithmetic contract
+
+// exp(d) by the base change exp(d) = 2^(d * log2 e): one round-to-nearest float32 multiply by
+// log2 e (rounded to float32), then the hardware base-2 approximation (PTX ex2.approx.f32,
+// which keeps subnormal results).  exp_fos(-inf) = +0.
+__device__ __forceinline__ float exp_fos(float d) {
+  const float t = __fmul_rn(d, 1.44269504088896340736f);
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+// exp(a - b) for a <= b, exactly 1 when a == b (both -inf included), 0 when only a is -inf.
+// Used wherever a rescale must be an exact no-op when the maximum does not move.
+__device__ __forceinline__ float scale_fos(float a, float b) {
+  return (a == b) ? 1.0f : exp_fos(__fsub_rn(a, b));
+}
+
+// Maximum over the 32 lanes (exact, so any tree gives the same value).
+__device__ __forceinline__ float warp_max_xor(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// Sum over the 32 lanes by the xor butterfly 16, 8, 4, 2, 1.  IEEE addition is commutative,
+// so every lane ends with the same bits.
+__device__ __forceinline__ float warp_sum_xor(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ dtype traits
+
+// Io<T>: raw storage of 8 keys (Raw), exact widening to float, and the single rounding of a
+// float result back to T (round to nearest even).
+template <typename T>
+struct Io;
+
+template <>
+struct Io<float> {
+  static constexpr int kEsz = 4;
+  struct Raw { float4 a, b; };
+  __device__ __forceinline__ static Raw lds(const unsigned char *p) {
+    Raw r;
+    r.a = *reinterpret_cast<const float4 *>(p);
+    r.b = *reinterpret_cast<const float4 *>(p + 16);
+    return r;
+  }
+  __device__ __forceinline__ static void widen(const Raw &r, float (&x)[8]) {
+    x[0] = r.a.x; x[1] = r.a.y; x[2] = r.a.z; x[3] = r.a.w;
+    x[4] = r.b.x; x[5] = r.b.y; x[6] = r.b.z; x[7] = r.b.w;
+  }
+  __device__ __forceinline__ static void st8(void *g, const float (&v)[8]) {
+    float4 *q = reinterpret_cast<float4 *>(g);
+    q[0] = make_float4(v[0], v[1], v[2], v[3]);
+    q[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  __device__ __forceinline__ static void st1(void *g, float v) { *reinterpret_cast<float *>(g) = v; }
+};
+
+template <>
+struct Io<__nv_bfloat16> {
+  static constexpr int kEsz = 2;
+  using Raw = uint4;
+  __device__ __forceinline__ static Raw lds(const unsigned char *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+  }
+  // bf16 -> f32 widening is exact: the 16 bits become the high half of the float.
+  __device__ __forceinline__ static void widen(const Raw &r, float (&x)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  __device__ __forceinline__ static void st8(void *g, const float (&v)[8]) {
+    *reinterpret_cast<uint4 *>(g) =
+        make_uint4(pack(v[0], v[1]), pack(v[2], v[3]), pack(v[4], v[5]), pack(v[6], v[7]));
+  }
+  __device__ __forceinline__ static void st1(void *g, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(g) = __float2bfloat16_rn(v);
+  }
+};
+
+template <>
+struct Io<__half> {
+  static constexpr int kEsz = 2;
+  using Raw = uint4;
+  __device__ __forceinline__ static Raw lds(const unsigned char *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+  }
+  __device__ __forceinline__ static void widen(const Raw &r, float (&x)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+      float2 f = __half22float2(h);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  __device__ __forceinline__ static void st8(void *g, const float (&v)[8]) {
+    *reinterpret_cast<uint4 *>(g) =
+        make_uint4(pack(v[0], v[1]), pack(v[2], v[3]), pack(v[4], v[5]), pack(v[6], v[7]));
+  }
+  __device__ __forceinline__ static void st1(void *g, float v) {
+    *reinterpret_cast<__half *>(g) = __float2half_rn(v);
+  }
+};
+
+// Store the 8 results of one lane (keys j0..j0+7) to a row of the output.  `vec` says the row
+// start is 16-byte aligned; keys at or beyond L are not written.
+template <typename T>
+__device__ __forceinline__ void store_lane8(unsigned char *row, int j0, int L, bool vec,
+                                            const float (&v)[8]) {
+  constexpr int esz = Io<T>::kEsz;
+  if (vec && j0 + kLaneKeys <= L) {
+    Io<T>::st8(row + (size_t)j0 * esz, v);
+  } else {
+#pragma unroll
+    for (int q = 0; q < kLaneKeys; ++q)
+      if (j0 + q < L) Io<T>::st1(row + (size_t)(j0 + q) * esz, v[q]);
+  }
+}
+
+// ------------------------------------------------------------------ row geometry and masks
+
+// Rows are ordered [batch][heads][q_len].  Returns the number of leading keys of row r that
+// can be valid (causal bound and valid length); key_mask and -inf are applied per key.
+__device__ __forceinline__ int row_limit(int64_t r, int L, int heads, int q_len, int causal,
+                                         const int32_t *kv_valid_len, int *b_out, int *h_out) {
+  const int64_t hs = (int64_t)heads * q_len;
+  const int b = (int)(r / hs);
+  const int h = (int)((r / q_len) % heads);
+  const int i = (int)(r % q_len);
+  int lim = L;
+  if (causal) lim = min(lim, L - q_len + i + 1);
+  if (kv_valid_len) lim = min(lim, max(0, min(kv_valid_len[b], L)));
+  *b_out = b;
+  *h_out = h;
+  return lim;
+}
+
+// ------------------------------------------------------------------ mbarrier + bulk copy
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.  Both addresses
+// must be 16-byte aligned and bytes a multiple of 16 (checked by the host launchers).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`, giving up after timeout_ns of the global timer or, should
+// the timer not advance, after a fixed number of polls.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  const uint64_t max_polls = (timeout_ns >> 4) + 1000000ull;
+  for (uint64_t n = 0; n < max_polls; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > timeout_ns) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void raise_device_error(unsigned *err, unsigned code) {
+  *reinterpret_cast<volatile unsigned *>(err) = code;
+}
+
+}  // namespace fos

@@ -1,0 +1,73 @@
+// fos_internal.h -- host/device interface between the C ABI (fos_api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/fos_softmax.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fos_softmax.h"
+
+namespace fos {
+
+constexpr int kTileK = 256;  // keys per tile: part of the arithmetic contract
+
+// Geometry and masks shared by the forward and backward row kernels.
+struct RowArgs {
+  int64_t rows;
+  int64_t ld;                  // elements between row starts
+  int32_t L;                   // key length
+  int32_t heads, q_len, causal;
+  const int32_t *kv_valid_len; // [batch] or null
+  const uint8_t *key_mask;     // [batch * L] or null
+  int32_t T;                   // tiles per row, ceil(L / 256)
+  int32_t stages;              // rows in flight per CTA (bulk-copy path); 1 on the plain path
+  uint32_t stage_bytes;        // shared-memory bytes of one staged input row (T * 256 * esz)
+  int32_t use_bulk;            // 1: 1-D bulk copies (TMA) into the ring; 0: plain loads
+  int32_t in_vec;              // input rows start 16-byte aligned
+  int32_t out_vec;             // output rows start 16-byte aligned
+  uint64_t timeout_ns;         // limit of every bounded wait
+  int32_t test_stall;          // test only: CTA 0 never issues its first copy
+  unsigned *err;               // device error word
+};
+
+struct FwdArgs : RowArgs {
+  const void *scores;
+  void *probs;
+  float *lse;
+  const float *sink;  // [heads] or null
+};
+
+struct BwdArgs : RowArgs {
+  const void *probs;
+  const void *dprobs;
+  void *dscores;
+  float *delta;  // [rows] or null
+};
+
+struct SinkArgs {
+  int32_t batch, heads, q_len;
+  const float *sink;
+  const float *lse;
+  const float *delta;
+  float *d_sink;
+};
+
+// Shared memory used by a row kernel besides its ring of staged rows.
+size_t fwd_extra_smem(int T, int stages);
+size_t bwd_extra_smem(int T, int stages);
+
+// Kernel instances per dtype: set the dynamic shared-memory limit, query residency, launch.
+cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
+cudaError_t fwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t fwd_launch(fos_dtype dt, const FwdArgs &a, int grid, int threads, size_t smem,
+                       cudaStream_t s);
+
+cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
+cudaError_t bwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t bwd_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                       cudaStream_t s);
+
+cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
+
+}  // namespace fos

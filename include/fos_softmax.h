@@ -1,0 +1,173 @@
+/*
+ * fos_softmax.h -- C ABI of libfos_softmax.so: a fixed-order, batch-invariant row softmax
+ * (forward, backward, per-head sink gradient) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation sits between the QK and AV GEMMs of joint attention: it takes a
+ * materialised score matrix, applies softmax along the key dimension and hands the
+ * probabilities on ("[WS1][kernels] Add fixed-order joint-attention softmax for Qwen-Image",
+ * Summary).  Its floating-point evaluation order is fixed, so a row gives the same bits
+ * whatever its batch, its position in the batch or the launch geometry (same page, Summary:
+ * "Fixed-order online softmax"; "Batch-invariant attention (standard softmax--cuda
+ * version)", Acceptance Criteria).
+ *
+ * Layout.  Scores, P, dP and dScores are row-major [rows, ld] arrays of the I/O dtype, with
+ * rows ordered [batch][heads][q_len] (row r has b = r / (heads*q_len), h = (r / q_len) %
+ * heads, i = r % q_len) and ld >= key_len elements between row starts.  Columns key_len ..
+ * ld-1 are never read or written.  LSE and delta are float32 [rows]; sink and d_sink are
+ * float32 [heads].
+ *
+ * Masks.  Key j of row r is valid iff all of the given conditions hold:
+ *   causal:        j <= key_len - q_len + i
+ *                  ("Batch-invariant attention", Prefill / Decode / KV-cache Contract)
+ *   kv_valid_len:  j <  kv_valid_len[b]   (values are clamped to [0, key_len])
+ *   key_mask:      key_mask[b*key_len + j] != 0
+ *   forward only:  scores[r, j] != -inf   (an input -inf acts as masked)
+ * Masked keys take no part in any sum and their P / dScores are written as +0.
+ * Scores equal to +inf or NaN are outside the contract (their rows come out NaN).
+ *
+ * Arithmetic contract (the same in every path of the library, so results are bit-identical
+ * across batch size, row offset, CTAs, warps per CTA, pipeline depth and load path):
+ *   - keys are cut into tiles of 256 (TILE_K), walked left to right; inside a tile lane l of
+ *     a warp owns keys 8l..8l+7 and combines them in ascending order, and the 32 lane values
+ *     are combined by a warp xor-shuffle tree with offsets 16, 8, 4, 2, 1;
+ *   - exp(x) is evaluated as 2^(x * log2 e) with the hardware base-2 approximation
+ *     (PTX ex2.approx.f32) after one float32 multiply by log2 e rounded to float32;
+ *   - all intermediates are float32 with explicit round-to-nearest operations (no FMA
+ *     contraction, no fast-math, no atomics, no split of a row across CTAs, no tensor cores);
+ *   - the result is rounded to the I/O dtype once, at the final write.
+ * fos_contract_fingerprint() spells out the full contract as a string.
+ *
+ * Ownership and streams.  The caller owns every buffer; all array pointers are DEVICE
+ * pointers.  The library allocates no memory, keeps no per-call state and never synchronises
+ * (fos_device_error excepted): each call validates its arguments on the host, enqueues its
+ * kernel on `stream` on the current device and returns.  Output buffers must not overlap
+ * inputs, except that probs may equal scores and dscores may equal dprobs (in place).
+ *
+ * Errors.  Every entry point returns fos_status:
+ *   FOS_ERR_INVALID      bad arguments (null required pointer, rows != batch*heads*q_len,
+ *                        key_len < 1, ld < key_len, unknown dtype, causal with q_len >
+ *                        key_len, bad launch options); nothing is launched.
+ *   FOS_ERR_UNSUPPORTED  valid, but beyond what the kernels stage (a row longer than shared
+ *                        memory, or a forced load path the buffers do not allow).
+ *   FOS_ERR_CUDA         the launch failed (cudaGetLastError after the launch).
+ *   FOS_ERR_TIMEOUT      reported by fos_device_error(): a bounded wait inside a kernel ran
+ *                        out, the kernel stopped early and its outputs are not valid.
+ * rows == 0 is valid and launches nothing (the array pointers may then be NULL).
+ */
+#ifndef FOS_SOFTMAX_H
+#define FOS_SOFTMAX_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* I/O dtype of scores, P, dP and dScores. */
+typedef enum fos_dtype {
+  FOS_F32 = 0,  /* IEEE binary32 */
+  FOS_BF16 = 1, /* bfloat16; rounded to nearest-even once, at the final write */
+  FOS_F16 = 2   /* IEEE binary16; rounded to nearest-even once, at the final write */
+} fos_dtype;
+
+typedef enum fos_status {
+  FOS_OK = 0,
+  FOS_ERR_INVALID = 1,
+  FOS_ERR_UNSUPPORTED = 2,
+  FOS_ERR_CUDA = 3,
+  FOS_ERR_TIMEOUT = 4
+} fos_status;
+
+/* Problem description shared by the three operations. */
+typedef struct fos_desc {
+  int64_t rows;                /* batch * heads * q_len */
+  int64_t ld;                  /* elements between row starts, >= key_len */
+  int32_t key_len;             /* L, keys per row, >= 1 */
+  int32_t batch;               /* B */
+  int32_t heads;               /* H */
+  int32_t q_len;               /* Sq, query rows per (batch, head) */
+  int32_t causal;              /* 0 or 1; key j of query i valid iff j <= L - Sq + i */
+  int32_t reserved;            /* must be 0 */
+  const int32_t *kv_valid_len; /* device [batch] or NULL: keys j >= kv_valid_len[b] masked */
+  const uint8_t *key_mask;     /* device [batch * key_len] or NULL: 0 = masked */
+  const float *sink;           /* device [heads] or NULL: per-head sink logit (off-by-one) */
+} fos_desc;
+
+/*
+ * Optional launch options (pass NULL for the defaults).  None of them changes a result bit:
+ * they exist so that tests can vary the launch geometry and exercise the bounded-wait path.
+ */
+typedef struct fos_launch {
+  int32_t warps_per_cta; /* 0 = default (8); otherwise 1..16 */
+  int32_t ctas;          /* 0 = default (persistent: SMs x resident CTAs); else >= 1 */
+  int32_t stages;        /* 0 = default; rows in flight per CTA on the bulk-copy path, 1..16 */
+  int32_t load_path;     /* 0 = auto, 1 = bulk copy (TMA) only, 2 = plain loads only */
+  int64_t wait_timeout_ns; /* 0 = default (2 s): limit of every bounded wait in a kernel */
+  int32_t test_stall;    /* 0; 1 = CTA 0 waits on a copy that is never issued (test only) */
+  int32_t reserved;      /* must be 0 */
+} fos_launch;
+
+/*
+ * Forward.  For each row: tile statistics (max, sum of exp) over keys 256t..256t+255,
+ * online-softmax states merged left to right starting from (sink_h, 1) when a sink is given
+ * and (-inf, 0) otherwise; LSE = M + log(S); P_j = exp(x_j - m_t) * (exp(m_t - M) / S) for
+ * key j of tile t.  ("[WS1][kernels] Add fixed-order joint-attention softmax for
+ * Qwen-Image", Summary; LSE: "Batch-invariant attention", Implementation; sink: "[ROCm] Jax
+ * Add softmax sink (learnable off-by-one) support", Description.)
+ *   scores  device [rows, ld] of dtype        (input)
+ *   probs   device [rows, ld] of dtype        (output P; may equal scores)
+ *   lse     device float [rows]               (output; -inf for a row with nothing valid)
+ */
+fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
+                           void *probs, float *lse, cudaStream_t stream,
+                           const fos_launch *launch);
+
+/*
+ * Backward (softmax VJP on the P given): delta = sum_j P_j dP_j with the forward's tile
+ * layout (lane-local ascending fused multiply-adds, warp xor tree, tile partials added left
+ * to right); dScores_j = P_j * (dP_j - delta), rounded once.  Only the mask inputs of desc
+ * are used (the sink is not).  ("[WS1][kernels] Add fixed-order joint-attention softmax for
+ * Qwen-Image", Summary, "Fixed-order backward".)
+ *   probs    device [rows, ld] of dtype      (input P)
+ *   dprobs   device [rows, ld] of dtype      (input dP)
+ *   dscores  device [rows, ld] of dtype      (output; may equal dprobs)
+ *   delta    device float [rows] or NULL     (output; needed later by fos_sink_grad)
+ */
+fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *probs,
+                           const void *dprobs, void *dscores, float *delta,
+                           cudaStream_t stream, const fos_launch *launch);
+
+/*
+ * Sink gradient: d_sink[h] = -sum_r exp(sink_h - lse_r) * delta_r over the rows of head h,
+ * taken in (b, i) order in chunks of 256 rows (lane-local ascending sums of 8, warp xor
+ * tree, chunk partials added left to right); no atomics.  A head whose sink is -inf gets 0.
+ * ("[ROCm] Jax Add softmax sink (learnable off-by-one) support": one sink value per head,
+ * d_sink reduced per head; the CK code there accumulates with atomicAdd, which this
+ * replaces by a fixed order.)
+ *   desc->sink must be non-NULL (FOS_ERR_INVALID otherwise).
+ *   lse, delta  device float [rows]  (inputs, as written by the forward and the backward)
+ *   d_sink      device float [heads] (output)
+ */
+fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
+                         float *d_sink, cudaStream_t stream, const fos_launch *launch);
+
+/*
+ * Synchronises `stream`, then reports and clears the device error word of the current
+ * device: FOS_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call, FOS_OK
+ * otherwise (FOS_ERR_CUDA if the synchronisation itself failed).
+ */
+fos_status fos_device_error(cudaStream_t stream);
+
+/* Static, NUL-terminated name of a status. */
+const char *fos_status_string(fos_status status);
+
+/* Static string naming the arithmetic contract: tile, lane layout, trees, exp form, arch. */
+const char *fos_contract_fingerprint(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOS_SOFTMAX_H */

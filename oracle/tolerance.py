@@ -1,0 +1,106 @@
+"""Parity tolerances between the CUDA library and the FP64 oracle -- TEST INFRASTRUCTURE ONLY.
+
+The bounds are the stated correctness bar of this build, read as follows (each reading is
+listed with its reason in the design notes):
+
+* P, float32 I/O: max |gpu - ref| <= 1e-6.
+* P, bf16/fp16 I/O: |gpu - ref| <= 1 ULP of the I/O dtype at the FP64 value.
+* LSE (float32 output for every I/O dtype): |gpu - ref| <= 1e-5 * max(1, |ref|); -inf exactly.
+* dScores: "1e-5 relative" is taken relative to the element's condition scale
+  s_j = |ref_j| + P_j * (|dP_j| + sum_k P_k |dP_k|), because dP_j - delta cancels.
+  float32 I/O: |err| <= 1e-5 * s_j;  bf16/fp16 I/O: |err| <= 1 ULP(ref_j) + 1e-5 * s_j.
+* delta (float32): |err| <= 1e-5 * sum_k P_k |dP_k|.
+* d_sink (float32): |err| <= 1e-5 * sum_r |c_r| with c_r = exp(sink_h - LSE_r) * delta_r.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+_MANT = {"float32": 23, "bfloat16": 7, "float16": 10}
+_EMIN = {"float32": -126, "bfloat16": -126, "float16": -14}
+
+
+def ulp(ref, dtype: str):
+    """Spacing of the I/O dtype's numbers at |ref| (ref in float64)."""
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    m, emin = _MANT[dtype], _EMIN[dtype]
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, (e - m).astype(np.int64))
+
+
+def _worst(err, bound):
+    ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1), np.where(err > 0, np.inf, 0))
+    i = int(np.argmax(ratio)) if ratio.size else 0
+    return (float(ratio.ravel()[i]) if ratio.size else 0.0), i
+
+
+def check_probs(gpu, ref, dtype: str):
+    """Returns (ok, worst ratio err/bound, flat index of the worst element)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    bound = np.full_like(ref, 1e-6) if dtype == "float32" else ulp(ref, dtype)
+    w, i = _worst(err, bound)
+    return bool(np.all(err <= bound)), w, i
+
+
+def check_lse(gpu, ref):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    same_inf = np.array_equal(np.isneginf(gpu), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    err = np.abs(gpu[fin] - ref[fin])
+    bound = 1e-5 * np.maximum(1.0, np.abs(ref[fin]))
+    w, i = _worst(err, bound)
+    return bool(same_inf and np.all(np.isfinite(gpu[fin])) and np.all(err <= bound)), w, i
+
+
+def dscores_scale(probs, dprobs, ref, valid=None):
+    """s_j = |ref_j| + P_j (|dP_j| + sum_k P_k |dP_k|) over valid keys (all when valid=None)."""
+    p = np.asarray(probs, dtype=np.float64)
+    dp = np.asarray(dprobs, dtype=np.float64)
+    pdp = np.abs(p * dp)
+    if valid is not None:
+        pdp = np.where(valid, pdp, 0.0)
+    row = pdp.sum(axis=-1, keepdims=True)
+    return np.abs(ref) + np.abs(p) * (np.abs(dp) + row), row[..., 0]
+
+
+def check_dscores(gpu, ref, probs, dprobs, dtype: str, valid=None):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    s, _ = dscores_scale(probs, dprobs, ref, valid)
+    bound = 1e-5 * s + 1e-30
+    if dtype != "float32":
+        bound = bound + ulp(ref, dtype)
+    err = np.abs(gpu - ref)
+    w, i = _worst(err, bound)
+    return bool(np.all(err <= bound)), w, i
+
+
+def check_delta(gpu, ref, probs, dprobs, valid=None):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    _, row = dscores_scale(probs, dprobs, np.zeros_like(np.asarray(probs, dtype=np.float64)), valid)
+    bound = 1e-5 * row + 1e-30
+    err = np.abs(gpu - ref)
+    w, i = _worst(err, bound)
+    return bool(np.all(err <= bound)), w, i
+
+
+def check_dsink(gpu, ref, lse, delta, sink, batch, heads, q_len):
+    """Bound 1e-5 * sum_r |exp(sink_h - LSE_r) * delta_r| per head (the oracle's LSE/delta)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64).reshape(batch, heads, q_len)
+    delta = np.asarray(delta, dtype=np.float64).reshape(batch, heads, q_len)
+    sk = np.asarray(sink, dtype=np.float64).reshape(1, heads, 1)
+    with np.errstate(invalid="ignore", over="ignore"):
+        c = np.where(np.isneginf(sk), 0.0, np.exp(sk - lse) * delta)
+    bound = 1e-5 * np.abs(c).sum(axis=(0, 2)) + 1e-30
+    err = np.abs(gpu - ref)
+    w, i = _worst(err, bound)
+    return bool(np.all(err <= bound)), w, i

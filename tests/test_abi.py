@@ -1,0 +1,127 @@
+"""The C-ABI library: it builds, loads, exports every symbol the header declares, and its host
+argument checks reject bad calls before touching CUDA (no GPU needed, no kernel launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "fos_softmax.h")
+
+
+@pytest.fixture(scope="module")
+def abi():
+    import deterministic_attention_softmax_gb300 as fos
+    from deterministic_attention_softmax_gb300 import _abi
+
+    fos.build()
+    return _abi
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(fos_[a-z_]+)\s*\(", text))
+
+
+def test_header_declares_the_binding_names(abi):
+    assert declared_functions() == set(abi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(abi):
+    lib = abi.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared but not exported"
+
+
+def test_struct_layout_matches_the_header(abi):
+    # fos_desc: 2 x int64, 6 x int32, 3 pointers; fos_launch: 4 x int32, int64, 2 x int32
+    assert ctypes.sizeof(abi.FosDesc) == 64
+    assert abi.FosDesc.kv_valid_len.offset == 40
+    assert ctypes.sizeof(abi.FosLaunch) == 32
+    assert abi.FosLaunch.wait_timeout_ns.offset == 16
+
+
+def test_status_strings_and_fingerprint(abi):
+    lib = abi.lib()
+    for code, name in abi.STATUS_NAMES.items():
+        assert lib.fos_status_string(code).decode().startswith(name)
+    fp = lib.fos_contract_fingerprint().decode()
+    for part in ("TILE_K=256", "xor tree 16,8,4,2,1", "sm_103a", "no atomics", "no fast-math"):
+        assert part in fp
+
+
+def _desc(abi, **kw):
+    d = dict(rows=6, ld=8, key_len=8, batch=1, heads=2, q_len=3, causal=0, reserved=0,
+             kv_valid_len=None, key_mask=None, sink=None)
+    d.update(kw)
+    return abi.FosDesc(**d)
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("bad", [
+    dict(rows=7),                    # rows != batch*heads*q_len
+    dict(key_len=0, ld=0),           # no keys
+    dict(ld=7),                      # ld < key_len
+    dict(causal=2),
+    dict(causal=1, q_len=9, rows=18, key_len=8),  # causal needs q_len <= key_len
+    dict(reserved=1),
+    dict(batch=-1, rows=-6),
+])
+def test_fwd_rejects_bad_descriptors(abi, bad):
+    d = _desc(abi, **bad)
+    st = abi.lib().fos_softmax_fwd(ctypes.byref(d), abi.FOS_BF16, FAKE, FAKE, FAKE, None, None)
+    assert st == abi.FOS_ERR_INVALID
+
+
+def test_rejects_null_pointers_and_bad_dtype(abi):
+    lib = abi.lib()
+    d = _desc(abi)
+    assert lib.fos_softmax_fwd(None, abi.FOS_BF16, FAKE, FAKE, FAKE, None, None) == abi.FOS_ERR_INVALID
+    assert lib.fos_softmax_fwd(ctypes.byref(d), 7, FAKE, FAKE, FAKE, None, None) == abi.FOS_ERR_INVALID
+    assert lib.fos_softmax_fwd(ctypes.byref(d), abi.FOS_F32, None, FAKE, FAKE, None, None) == abi.FOS_ERR_INVALID
+    assert lib.fos_softmax_fwd(ctypes.byref(d), abi.FOS_F32, FAKE, FAKE, None, None, None) == abi.FOS_ERR_INVALID
+    assert lib.fos_softmax_bwd(ctypes.byref(d), abi.FOS_F32, FAKE, None, FAKE, None, None, None) == abi.FOS_ERR_INVALID
+    # the sink gradient needs a sink (a null sink with a sink operation is an error, not a no-op)
+    assert lib.fos_sink_grad(ctypes.byref(d), FAKE, FAKE, FAKE, None, None) == abi.FOS_ERR_INVALID
+
+
+@pytest.mark.parametrize("bad", [
+    dict(warps_per_cta=17), dict(warps_per_cta=-1), dict(ctas=-2), dict(stages=17),
+    dict(load_path=3), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(reserved=1),
+])
+def test_rejects_bad_launch_options(abi, bad):
+    opts = dict(warps_per_cta=0, ctas=0, stages=0, load_path=0, wait_timeout_ns=0, test_stall=0,
+                reserved=0)
+    opts.update(bad)
+    lc = abi.FosLaunch(**opts)
+    d = _desc(abi)
+    st = abi.lib().fos_softmax_fwd(ctypes.byref(d), abi.FOS_BF16, FAKE, FAKE, FAKE, None,
+                                   ctypes.byref(lc))
+    assert st == abi.FOS_ERR_INVALID
+
+
+def test_zero_rows_is_ok_and_launches_nothing(abi):
+    d = _desc(abi, rows=0, batch=0)
+    st = abi.lib().fos_softmax_fwd(ctypes.byref(d), abi.FOS_BF16, FAKE, FAKE, FAKE, None, None)
+    assert st == abi.FOS_OK
+    st = abi.lib().fos_softmax_bwd(ctypes.byref(d), abi.FOS_BF16, FAKE, FAKE, FAKE, None, None, None)
+    assert st == abi.FOS_OK
+    # empty tensors may have null data pointers
+    st = abi.lib().fos_softmax_fwd(ctypes.byref(d), abi.FOS_BF16, None, None, None, None, None)
+    assert st == abi.FOS_OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    import deterministic_attention_softmax_gb300 as fos
+
+    fos.build()
+    with pytest.raises(ValueError):
+        fos.fos_softmax_fwd(torch.zeros(4, 8))
