@@ -166,6 +166,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   ra->out_vec = (stride16 && aligned16(output)) ? 1 : 0;
   ra->timeout_ns = (l && l->wait_timeout_ns) ? (uint64_t)l->wait_timeout_ns : kDefaultTimeoutNs;
   ra->test_stall = l ? l->test_stall : 0;
+  ra->need_geo = (d->causal || d->kv_valid_len || d->key_mask) ? 1 : 0;
   ra->err = dev.err;
 
   pl->threads = warps * 32;
@@ -196,15 +197,20 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
   FwdArgs a{};
   Plan pl;
   const void *inputs[1] = {scores};
+  const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
+  const int kt = fwd_tiles_per_warp((desc->key_len + kTileK - 1) / kTileK, warps);
   st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem,
-                 [dtype](int th, size_t sm, int *n) { return fwd_occupancy(dtype, th, sm, n); },
+                 [dtype, kt](int th, size_t sm, int *n) {
+                   return fwd_occupancy(dtype, kt, th, sm, n);
+                 },
                  &a, &pl);
   if (st != FOS_OK) return st;
   a.scores = scores;
   a.probs = probs;
   a.lse = lse;
   a.sink = desc->sink;
-  if (fwd_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+  if (desc->sink) a.need_geo = 1;  // the merge needs the row's head
+  if (fwd_launch(dtype, kt, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
     return FOS_ERR_CUDA;
   return FOS_OK;
 }

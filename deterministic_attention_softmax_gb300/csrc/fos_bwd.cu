@@ -12,37 +12,54 @@
 // difference, and rounded once.  Masked keys are skipped in the sum and written as +0.
 //
 // Structure as in the forward: persistent CTAs, a ring of staged rows (P and dP of a row
-// arrive by two 1-D bulk copies on one mbarrier), one CTA per row at a time; warp 0 adds the
-// tile partials, everything else is tile-parallel over the warps.
+// arrive by two 1-D bulk copies on one mbarrier), one CTA per row at a time; thread 0 adds the
+// tile partials, everything else is tile-parallel over the warps.  Pass 2 re-reads P and dP
+// from shared memory, so a stage is refilled once the next row's first barrier shows that
+// every warp is done with it (with a single stage: after an end-of-row barrier).
 #include "fos_device.cuh"
 #include "fos_internal.h"
 
 namespace fos {
 namespace {
 
-constexpr int kKT = 4;          // tiles per warp whose P and dP stay in registers
-constexpr int kBarBytes = 128;  // room for up to 16 mbarriers at the start of smem
+constexpr int kBarBytes = 128;  // up to 16 mbarriers
+constexpr int kGeoBytes = 256;  // up to 16 per-stage row records (int4)
 
 __device__ __forceinline__ bool key_ok(int j, int lim, const uint8_t *km) {
   return (j < lim) && (km == nullptr || km[j] != 0);
 }
 
+template <typename T>
+__device__ __forceinline__ void tile_pdp(const unsigned char *sp, const unsigned char *sd, int j0,
+                                         float (&p)[8], float (&d)[8]) {
+  constexpr int esz = Io<T>::kEsz;
+  Io<T>::widen(Io<T>::lds(sp + (size_t)j0 * esz), p);
+  Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
+}
+
 // Lane-local ascending fused multiply-add over the lane's 8 keys, then the xor tree.
-__device__ __forceinline__ float tile_dot(const float (&p)[8], const float (&d)[8], int j0, int lim,
-                                          const uint8_t *km) {
+__device__ __forceinline__ float tile_dot(const float (&p)[8], const float (&d)[8], int j0,
+                                          int lim, const uint8_t *km, bool masked) {
   float acc = 0.0f;
+  if (masked) {
 #pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q)
-    if (key_ok(j0 + q, lim, km)) acc = __fmaf_rn(p[q], d[q], acc);
+    for (int q = 0; q < kLaneKeys; ++q)
+      if (key_ok(j0 + q, lim, km)) acc = __fmaf_rn(p[q], d[q], acc);
+  } else {
+#pragma unroll
+    for (int q = 0; q < kLaneKeys; ++q) acc = __fmaf_rn(p[q], d[q], acc);
+  }
   return warp_sum_xor(acc);
 }
 
 __device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[8], int j0,
-                                          int lim, const uint8_t *km, float delta,
+                                          int lim, const uint8_t *km, bool masked, float delta,
                                           float (&v)[8]) {
 #pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q)
-    v[q] = key_ok(j0 + q, lim, km) ? __fmaf_rn(p[q], __fsub_rn(d[q], delta), 0.0f) : 0.0f;
+  for (int q = 0; q < kLaneKeys; ++q) {
+    const float g = __fmaf_rn(p[q], __fsub_rn(d[q], delta), 0.0f);
+    v[q] = (!masked || key_ok(j0 + q, lim, km)) ? g : 0.0f;
+  }
 }
 
 template <typename T>
@@ -64,13 +81,15 @@ __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned
   }
 }
 
+// Thread 0: record row rr's geometry and start the bulk copies of its P and dP.
 template <typename T>
 __device__ __forceinline__ void issue_row(const BwdArgs &a, int64_t rr, unsigned char *stage,
-                                          uint64_t *bar) {
+                                          uint64_t *bar, int4 *geo, bool skip_copy) {
   constexpr int esz = Io<T>::kEsz;
-  int b, h;
-  const int lim = row_limit(rr, a.L, a.heads, a.q_len, a.causal, a.kv_valid_len, &b, &h);
-  const uint32_t bytes = ((uint32_t)lim * esz + 15u) & ~15u;
+  const int4 g = row_geometry(a, rr);
+  *geo = g;
+  const uint32_t bytes = ((uint32_t)g.x * esz + 15u) & ~15u;
+  if (skip_copy) return;  // test only: this row's copies are never issued
   const uint32_t bar_a = smem_addr(bar);
   mbar_arrive_expect_tx(bar_a, 2u * bytes);
   if (bytes) {
@@ -82,12 +101,12 @@ __device__ __forceinline__ void issue_row(const BwdArgs &a, int64_t rr, unsigned
 }
 
 template <typename T>
-__global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
+__global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
-  using Raw = typename Io<T>::Raw;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-  unsigned char *ring = smem + kBarBytes;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes);
+  unsigned char *ring = smem + kBarBytes + kGeoBytes;
   const size_t slot = 2 * (size_t)a.stage_bytes;
   float *td = reinterpret_cast<float *>(ring + (size_t)a.stages * slot);
   float *dsm = td + a.T;  // delta of the current row, for every warp
@@ -102,6 +121,7 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
   const bool stall = a.test_stall && blockIdx.x == 0;
+  const bool defer = NS >= 2;  // refill a row's stage at the next row's first barrier
   int64_t issued_end = 0;
 
   if (a.use_bulk) {
@@ -110,10 +130,10 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
       fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0)
       for (int64_t kk = 0; kk < nmine && kk < NS; ++kk)
-        if (!(stall && kk == 0)) issue_row<T>(a, r0 + kk * G, ring + (size_t)kk * slot, &bars[kk]);
-    }
+        issue_row<T>(a, r0 + kk * G, ring + (size_t)kk * slot, &bars[kk], &geos[kk],
+                     stall && kk == 0);
     issued_end = nmine < NS ? nmine : NS;
   }
 
@@ -122,48 +142,33 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
     const int s = a.use_bulk ? (int)(k % NS) : 0;
     unsigned char *sp = ring + (size_t)s * slot;
     unsigned char *sd = sp + a.stage_bytes;
-    int b, h;
-    const int lim = row_limit(r, a.L, a.heads, a.q_len, a.causal, a.kv_valid_len, &b, &h);
-    const int Te = (lim + kTileK - 1) / kTileK;
-    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)b * a.L : nullptr;
-    const bool in_regs = Te <= nw * kKT;
 
     bool timed_out = false;
+    int4 g;
     if (a.use_bulk) {
       timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((k / NS) & 1), a.timeout_ns);
+      g = geos[s];
     } else {
+      if (tid == 0) geos[0] = row_geometry(a, r);
+      __syncthreads();  // also: every warp is done with the previous row's stage
+      g = geos[0];
       const size_t off = (size_t)r * a.ld * esz;
-      plain_stage<T>(sp, static_cast<const unsigned char *>(a.probs) + off, lim, a.in_vec != 0);
-      plain_stage<T>(sd, static_cast<const unsigned char *>(a.dprobs) + off, lim, a.in_vec != 0);
+      plain_stage<T>(sp, static_cast<const unsigned char *>(a.probs) + off, g.x, a.in_vec != 0);
+      plain_stage<T>(sd, static_cast<const unsigned char *>(a.dprobs) + off, g.x, a.in_vec != 0);
       __syncthreads();
     }
+    const int lim = g.x;
+    const int Te = (lim + kTileK - 1) / kTileK;
+    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: tile partials of delta
-    Raw rp[kKT], rd[kKT];
-    if (in_regs) {
-#pragma unroll
-      for (int kk = 0; kk < kKT; ++kk) {
-        const int t = w + kk * nw;
-        if (t < Te) {
-          const int j0 = t * kTileK + lane * kLaneKeys;
-          rp[kk] = Io<T>::lds(sp + (size_t)j0 * esz);
-          rd[kk] = Io<T>::lds(sd + (size_t)j0 * esz);
-          float p[8], d[8];
-          Io<T>::widen(rp[kk], p);
-          Io<T>::widen(rd[kk], d);
-          const float part = tile_dot(p, d, j0, lim, km);
-          if (lane == 0) td[t] = part;
-        }
-      }
-    } else {
-      for (int t = w; t < Te; t += nw) {
-        const int j0 = t * kTileK + lane * kLaneKeys;
-        float p[8], d[8];
-        Io<T>::widen(Io<T>::lds(sp + (size_t)j0 * esz), p);
-        Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
-        const float part = tile_dot(p, d, j0, lim, km);
-        if (lane == 0) td[t] = part;
-      }
+    for (int t = w; t < Te; t += nw) {
+      const int j0 = t * kTileK + lane * kLaneKeys;
+      float p[8], d[8];
+      tile_pdp<T>(sp, sd, j0, p, d);
+      const bool masked = km != nullptr || (t + 1) * kTileK > lim;
+      const float part = tile_dot(p, d, j0, lim, km, masked);
+      if (lane == 0) td[t] = part;
     }
 
     if (__syncthreads_or(timed_out)) {
@@ -177,13 +182,14 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
       return;
     }
 
-    if (a.use_bulk && in_regs && tid == 0 && k + NS < nmine) {
-      issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s]);
-      issued_end = k + NS + 1;
-    }
-
-    // ---- tile partials added left to right (one thread)
+    // ---- tile partials added left to right; the previous row's stage is free now
     if (tid == 0) {
+      if (a.use_bulk && defer && k >= 1 && k - 1 + NS < nmine) {
+        const int sr = (int)((k - 1) % NS);
+        issue_row<T>(a, r0 + (k - 1 + NS) * G, ring + (size_t)sr * slot, &bars[sr], &geos[sr],
+                     false);
+        issued_end = k + NS;
+      }
       float delta = 0.0f;
       for (int t = 0; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
       dsm[0] = delta;
@@ -195,28 +201,13 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
     // ---- pass 2: dScores
     unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
     const bool ovec = a.out_vec != 0;
-    if (in_regs) {
-#pragma unroll
-      for (int kk = 0; kk < kKT; ++kk) {
-        const int t = w + kk * nw;
-        if (t < Te) {
-          const int j0 = t * kTileK + lane * kLaneKeys;
-          float p[8], d[8], v[8];
-          Io<T>::widen(rp[kk], p);
-          Io<T>::widen(rd[kk], d);
-          tile_grad(p, d, j0, lim, km, delta, v);
-          store_lane8<T>(grow, j0, a.L, ovec, v);
-        }
-      }
-    } else {
-      for (int t = w; t < Te; t += nw) {
-        const int j0 = t * kTileK + lane * kLaneKeys;
-        float p[8], d[8], v[8];
-        Io<T>::widen(Io<T>::lds(sp + (size_t)j0 * esz), p);
-        Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
-        tile_grad(p, d, j0, lim, km, delta, v);
-        store_lane8<T>(grow, j0, a.L, ovec, v);
-      }
+    for (int t = w; t < Te; t += nw) {
+      const int j0 = t * kTileK + lane * kLaneKeys;
+      float p[8], d[8], v[8];
+      tile_pdp<T>(sp, sd, j0, p, d);
+      const bool masked = km != nullptr || (t + 1) * kTileK > lim;
+      tile_grad(p, d, j0, lim, km, masked, delta, v);
+      store_lane8<T>(grow, j0, a.L, ovec, v);
     }
     for (int t = Te + w; t < a.T; t += nw) {
       float z[8];
@@ -225,10 +216,10 @@ __global__ void __launch_bounds__(512, 1) fos_bwd_kernel(const BwdArgs a) {
       store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
     }
 
-    if (!in_regs) {
-      __syncthreads();
+    if (!defer) {
+      __syncthreads();  // single stage: everyone is done with it before it is refilled
       if (a.use_bulk && tid == 0 && k + NS < nmine) {
-        issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s]);
+        issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s], &geos[s], false);
         issued_end = k + NS + 1;
       }
     }
@@ -248,7 +239,7 @@ const void *bwd_fn(fos_dtype dt) {
 
 size_t bwd_extra_smem(int T, int stages) {
   (void)stages;
-  return (size_t)kBarBytes + (size_t)(T + 4) * sizeof(float);
+  return (size_t)kBarBytes + kGeoBytes + (size_t)(T + 4) * sizeof(float);
 }
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {

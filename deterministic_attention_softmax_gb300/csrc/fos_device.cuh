@@ -163,20 +163,32 @@ __device__ __forceinline__ void store_lane8(unsigned char *row, int j0, int L, b
 
 // ------------------------------------------------------------------ row geometry and masks
 
-// Rows are ordered [batch][heads][q_len].  Returns the number of leading keys of row r that
-// can be valid (causal bound and valid length); key_mask and -inf are applied per key.
-__device__ __forceinline__ int row_limit(int64_t r, int L, int heads, int q_len, int causal,
-                                         const int32_t *kv_valid_len, int *b_out, int *h_out) {
-  const int64_t hs = (int64_t)heads * q_len;
-  const int b = (int)(r / hs);
-  const int h = (int)((r / q_len) % heads);
-  const int i = (int)(r % q_len);
-  int lim = L;
-  if (causal) lim = min(lim, L - q_len + i + 1);
-  if (kv_valid_len) lim = min(lim, max(0, min(kv_valid_len[b], L)));
-  *b_out = b;
-  *h_out = h;
-  return lim;
+// Rows are ordered [batch][heads][q_len].  Returns {lim, b, h, 0}: lim is the number of
+// leading keys of row r that can be valid (causal bound and valid length; key_mask and -inf
+// are applied per key), b and h its batch entry and head.  Only computed when a mask or a
+// sink needs it (one thread per row calls this, when it issues the row's copy).
+__device__ __forceinline__ int4 row_geometry(const RowArgs &a, int64_t r) {
+  int4 g = make_int4(a.L, 0, 0, 0);
+  if (!a.need_geo) return g;
+  int64_t b, h, i;
+  if (a.rows <= 0x7fffffffLL) {  // 32-bit arithmetic suffices
+    const uint32_t rr = (uint32_t)r, q = rr / (uint32_t)a.q_len;
+    i = rr - q * (uint32_t)a.q_len;
+    b = q / (uint32_t)a.heads;
+    h = q - (uint32_t)b * (uint32_t)a.heads;
+  } else {
+    const int64_t q = r / a.q_len;
+    i = r - q * a.q_len;
+    b = q / a.heads;
+    h = q - b * a.heads;
+  }
+  int lim = a.L;
+  if (a.causal) lim = min(lim, (int)(a.L - a.q_len + i + 1));
+  if (a.kv_valid_len) lim = min(lim, max(0, min(a.kv_valid_len[b], a.L)));
+  g.x = lim;
+  g.y = (int)b;
+  g.z = (int)h;
+  return g;
 }
 
 // ------------------------------------------------------------------ mbarrier + bulk copy

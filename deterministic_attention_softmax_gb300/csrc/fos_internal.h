@@ -28,6 +28,7 @@ struct RowArgs {
   int32_t out_vec;             // output rows start 16-byte aligned
   uint64_t timeout_ns;         // limit of every bounded wait
   int32_t test_stall;          // test only: CTA 0 never issues its first copy
+  int32_t need_geo;            // rows need b / h / limit (a mask or a sink is given)
   unsigned *err;               // device error word
 };
 
@@ -58,10 +59,12 @@ size_t fwd_extra_smem(int T, int stages);
 size_t bwd_extra_smem(int T, int stages);
 
 // Kernel instances per dtype: set the dynamic shared-memory limit, query residency, launch.
+// The forward keeps e_j of `kt` tiles per warp in registers (kt = 4 or 8).
+int fwd_tiles_per_warp(int T, int warps);
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
-cudaError_t fwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
-cudaError_t fwd_launch(fos_dtype dt, const FwdArgs &a, int grid, int threads, size_t smem,
-                       cudaStream_t s);
+cudaError_t fwd_occupancy(fos_dtype dt, int kt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t fwd_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
+                       size_t smem, cudaStream_t s);
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t bwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
