@@ -49,7 +49,7 @@ class FosLaunch(ctypes.Structure):
         ("load_path", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
         ("test_stall", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("generic", ctypes.c_int32),
     ]
 
 

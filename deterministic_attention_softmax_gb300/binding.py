@@ -43,10 +43,11 @@ class Launch:
     load_path: int = 0  # 0 auto, 1 bulk copy (TMA) only, 2 plain loads only
     wait_timeout_ns: int = 0
     test_stall: int = 0
+    generic: int = 0  # 1: never the kernel specialised for the common case
 
     def _c(self) -> _abi.FosLaunch:
         return _abi.FosLaunch(self.warps_per_cta, self.ctas, self.stages, self.load_path,
-                              self.wait_timeout_ns, self.test_stall, 0)
+                              self.wait_timeout_ns, self.test_stall, self.generic)
 
 
 def _rows_layout(t: torch.Tensor, name: str):

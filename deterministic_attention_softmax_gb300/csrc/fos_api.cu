@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kBarBytes = 128;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultWarps = 8;
-constexpr size_t kStageTarget = 64 * 1024;  // ring bytes per CTA aimed at by default
+constexpr size_t kStageTarget = 48 * 1024;  // ring bytes per CTA aimed at by default
 constexpr int kMaxStages = 16;
 
 struct DevInfo {
@@ -92,7 +92,7 @@ fos_status check_launch(const fos_launch *l) {
   if (l->load_path < 0 || l->load_path > 2) return FOS_ERR_INVALID;
   if (l->wait_timeout_ns < 0) return FOS_ERR_INVALID;
   if (l->test_stall != 0 && l->test_stall != 1) return FOS_ERR_INVALID;
-  if (l->reserved != 0) return FOS_ERR_INVALID;
+  if (l->generic != 0 && l->generic != 1) return FOS_ERR_INVALID;
   return FOS_OK;
 }
 
@@ -110,7 +110,8 @@ struct Plan {
 template <typename OccFn>
 fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
-                     size_t (*extra)(int, int), OccFn occ, RowArgs *ra, Plan *pl) {
+                     size_t (*extra)(int, int), int default_warps, OccFn occ, RowArgs *ra,
+                     Plan *pl) {
   const int esz = dtype_size(dt);
   const int T = (d->key_len + kTileK - 1) / kTileK;
   const size_t stage_bytes = (size_t)T * kTileK * esz;
@@ -122,7 +123,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   if (path == 1 && !bulk_ok) return FOS_ERR_UNSUPPORTED;
   const bool bulk = (path == 1) || (path == 0 && bulk_ok);
 
-  const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : kDefaultWarps;
+  const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : default_warps;
   const size_t slot = (size_t)copies * stage_bytes;
   const size_t fixed = extra(T, 0);
   if (fixed + slot > (size_t)dev.max_smem) return FOS_ERR_UNSUPPORTED;
@@ -144,7 +145,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
     grid = l->ctas;
   } else {
     int per_sm = 0;
-    if (occ(warps * 32, smem, &per_sm) != cudaSuccess) return FOS_ERR_CUDA;
+    if (occ((warps + 1) * 32, smem, &per_sm) != cudaSuccess) return FOS_ERR_CUDA;
     if (per_sm < 1) return FOS_ERR_UNSUPPORTED;
     grid = per_sm * dev.sms;
   }
@@ -169,7 +170,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   ra->need_geo = (d->causal || d->kv_valid_len || d->key_mask) ? 1 : 0;
   ra->err = dev.err;
 
-  pl->threads = warps * 32;
+  pl->threads = (warps + 1) * 32;  // the compute warps and one producer warp
   pl->grid = grid;
   pl->smem = smem;
   pl->stages = stages;
@@ -197,11 +198,21 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
   FwdArgs a{};
   Plan pl;
   const void *inputs[1] = {scores};
-  const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
-  const int kt = fwd_tiles_per_warp((desc->key_len + kTileK - 1) / kTileK, warps);
-  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem,
-                 [dtype, kt](int th, size_t sm, int *n) {
-                   return fwd_occupancy(dtype, kt, th, sm, n);
+  const int T = (desc->key_len + kTileK - 1) / kTileK;
+  const int warps =
+      (launch && launch->warps_per_cta) ? launch->warps_per_cta : fwd_default_warps(T);
+  int kt = fwd_tiles_per_warp(T, warps);
+  const bool in_regs = T <= warps * kt;
+  if (!in_regs) kt = 2;  // e_j are recomputed: keep the register footprint small
+  // The specialised instance covers the common case; the generic one covers the rest.
+  const int esz = dtype_size(dtype);
+  const bool fast = in_regs && !(launch && launch->generic) && !(launch && launch->load_path == 2) &&
+                    !desc->causal && !desc->kv_valid_len && !desc->key_mask && !desc->sink &&
+                    aligned16(scores) && aligned16(probs) && ((desc->ld * esz) & 15) == 0 &&
+                    (((int64_t)desc->key_len * esz) & 15) == 0;
+  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem, warps,
+                 [dtype, kt, fast](int th, size_t sm, int *n) {
+                   return fwd_occupancy(dtype, kt, fast, th, sm, n);
                  },
                  &a, &pl);
   if (st != FOS_OK) return st;
@@ -210,7 +221,8 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
   a.lse = lse;
   a.sink = desc->sink;
   if (desc->sink) a.need_geo = 1;  // the merge needs the row's head
-  if (fwd_launch(dtype, kt, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+  if (fwd_launch(dtype, kt, fast && a.use_bulk && a.out_vec, a, pl.grid, pl.threads, pl.smem,
+                 stream) != cudaSuccess)
     return FOS_ERR_CUDA;
   return FOS_OK;
 }
@@ -231,6 +243,7 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
   Plan pl;
   const void *inputs[2] = {probs, dprobs};
   st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
+                 bwd_default_warps((desc->key_len + kTileK - 1) / kTileK),
                  [dtype](int th, size_t sm, int *n) { return bwd_occupancy(dtype, th, sm, n); },
                  &a, &pl);
   if (st != FOS_OK) return st;

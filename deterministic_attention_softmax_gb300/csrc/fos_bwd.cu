@@ -11,18 +11,18 @@
 // as fma(P_j, dP_j - delta, +0) so that a zero product is +0 whatever the sign of the
 // difference, and rounded once.  Masked keys are skipped in the sum and written as +0.
 //
-// Structure as in the forward: persistent CTAs, a ring of staged rows (P and dP of a row
-// arrive by two 1-D bulk copies on one mbarrier), one CTA per row at a time; thread 0 adds the
-// tile partials, everything else is tile-parallel over the warps.  Pass 2 re-reads P and dP
-// from shared memory, so a stage is refilled once the next row's first barrier shows that
-// every warp is done with it (with a single stage: after an end-of-row barrier).
+// Structure as in the forward: persistent CTAs, a producer warp that alone issues the 1-D bulk
+// copies (P and dP of a row on one mbarrier) into a ring of staged rows, compute warps that
+// own one complete row at a time; thread 0 adds the tile partials, everything else is
+// tile-parallel over the compute warps.  Pass 2 re-reads P and dP from shared memory, and each
+// compute warp releases the stage to the producer when its pass 2 is done.
 #include "fos_device.cuh"
 #include "fos_internal.h"
 
 namespace fos {
 namespace {
 
-constexpr int kBarBytes = 128;  // up to 16 mbarriers
+constexpr int kBarBytes = 256;  // 16 "full" and 16 "empty" mbarriers
 constexpr int kGeoBytes = 256;  // up to 16 per-stage row records (int4)
 
 __device__ __forceinline__ bool key_ok(int j, int lim, const uint8_t *km) {
@@ -37,8 +37,8 @@ __device__ __forceinline__ void tile_pdp(const unsigned char *sp, const unsigned
   Io<T>::widen(Io<T>::lds(sd + (size_t)j0 * esz), d);
 }
 
-// Lane-local ascending fused multiply-add over the lane's 8 keys, then the xor tree.
-__device__ __forceinline__ float tile_dot(const float (&p)[8], const float (&d)[8], int j0,
+// Lane-local ascending fused multiply-add over the lane's 8 keys (the xor tree follows).
+__device__ __forceinline__ float lane_dot(const float (&p)[8], const float (&d)[8], int j0,
                                           int lim, const uint8_t *km, bool masked) {
   float acc = 0.0f;
   if (masked) {
@@ -49,7 +49,7 @@ __device__ __forceinline__ float tile_dot(const float (&p)[8], const float (&d)[
 #pragma unroll
     for (int q = 0; q < kLaneKeys; ++q) acc = __fmaf_rn(p[q], d[q], acc);
   }
-  return warp_sum_xor(acc);
+  return acc;
 }
 
 __device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[8], int j0,
@@ -64,16 +64,16 @@ __device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[
 
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
-                                            int lim, bool vec) {
+                                            int lim, bool vec, int nthreads) {
   constexpr int esz = Io<T>::kEsz;
   int start = 0;
   if (vec) {
     const int n16 = (lim * esz) >> 4;
-    for (int c = threadIdx.x; c < n16; c += blockDim.x)
+    for (int c = threadIdx.x; c < n16; c += nthreads)
       reinterpret_cast<uint4 *>(stage)[c] = reinterpret_cast<const uint4 *>(src)[c];
     start = (n16 << 4) / esz;
   }
-  for (int j = start + threadIdx.x; j < lim; j += blockDim.x) {
+  for (int j = start + threadIdx.x; j < lim; j += nthreads) {
     if (esz == 4)
       reinterpret_cast<uint32_t *>(stage)[j] = reinterpret_cast<const uint32_t *>(src)[j];
     else
@@ -100,19 +100,53 @@ __device__ __forceinline__ void issue_row(const BwdArgs &a, int64_t rr, unsigned
   }
 }
 
+// Producer (lane 0 of the last warp): as in the forward, it alone issues the bulk copies
+// (P and dP of a row on one "full" barrier) once the compute warps have released the stage,
+// and waits for every copy it issued before it exits.
+template <typename T>
+__device__ void bwd_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
+                            uint64_t *full, uint64_t *empty, int4 *geos, unsigned char *ring,
+                            size_t slot, bool stall) {
+  const int NS = a.stages;
+  uint32_t issued = 0, last_ph = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t kk = 0; kk < nmine; ++kk) {
+    if (kk >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, a.timeout_ns)) {
+      raise_device_error(a.err, kDevErrTimeout);
+      break;
+    }
+    const bool skip = stall && kk == 0;
+    issue_row<T>(a, r0 + kk * G, ring + (size_t)s * slot, &full[s], &geos[s], skip);
+    if (!skip) {
+      issued |= 1u << s;
+      last_ph = (last_ph & ~(1u << s)) | (ph << s);
+    }
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  for (int t = 0; t < NS; ++t)
+    if (issued & (1u << t))
+      mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
 template <typename T>
 __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + 16;
   int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes);
   unsigned char *ring = smem + kBarBytes + kGeoBytes;
   const size_t slot = 2 * (size_t)a.stage_bytes;
   float *td = reinterpret_cast<float *>(ring + (size_t)a.stages * slot);
-  float *dsm = td + a.T;  // delta of the current row, for every warp
+  float *dsm = td + ((a.T + 3) & ~3);  // delta of the current row, for every warp
 
   const int tid = threadIdx.x;
-  const int nw = blockDim.x >> 5;
+  const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
+  const int ncomp = nw * 32;
   const int w = tid >> 5;
   const int lane = tid & 31;
   const int64_t G = gridDim.x;
@@ -120,82 +154,98 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   if (r0 >= a.rows) return;
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
-  const bool stall = a.test_stall && blockIdx.x == 0;
-  const bool defer = NS >= 2;  // refill a row's stage at the next row's first barrier
-  int64_t issued_end = 0;
 
   if (a.use_bulk) {
     if (tid == 0) {
-      for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&bars[s]), 1);
+      for (int t = 0; t < NS; ++t) {
+        mbar_init(smem_addr(&full[t]), 1);
+        mbar_init(smem_addr(&empty[t]), nw);
+      }
       fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0)
-      for (int64_t kk = 0; kk < nmine && kk < NS; ++kk)
-        issue_row<T>(a, r0 + kk * G, ring + (size_t)kk * slot, &bars[kk], &geos[kk],
-                     stall && kk == 0);
-    issued_end = nmine < NS ? nmine : NS;
+  }
+  if (w == nw) {
+    if (a.use_bulk && lane == 0)
+      bwd_produce<T>(a, r0, G, nmine, full, empty, geos, ring, slot,
+                     a.test_stall && blockIdx.x == 0);
+    return;
   }
 
-  for (int64_t k = 0; k < nmine; ++k) {
+  // stage index and phase parity of row k, carried rather than computed
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t k = 0; k < nmine; ++k, s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
     const int64_t r = r0 + k * G;
-    const int s = a.use_bulk ? (int)(k % NS) : 0;
     unsigned char *sp = ring + (size_t)s * slot;
     unsigned char *sd = sp + a.stage_bytes;
 
     bool timed_out = false;
     int4 g;
     if (a.use_bulk) {
-      timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((k / NS) & 1), a.timeout_ns);
+      timed_out = !mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
       g = geos[s];
     } else {
       if (tid == 0) geos[0] = row_geometry(a, r);
-      __syncthreads();  // also: every warp is done with the previous row's stage
+      compute_sync(ncomp);  // also: every warp is done with the previous row's stage
       g = geos[0];
       const size_t off = (size_t)r * a.ld * esz;
-      plain_stage<T>(sp, static_cast<const unsigned char *>(a.probs) + off, g.x, a.in_vec != 0);
-      plain_stage<T>(sd, static_cast<const unsigned char *>(a.dprobs) + off, g.x, a.in_vec != 0);
-      __syncthreads();
+      plain_stage<T>(sp, static_cast<const unsigned char *>(a.probs) + off, g.x, a.in_vec != 0,
+                     ncomp);
+      plain_stage<T>(sd, static_cast<const unsigned char *>(a.dprobs) + off, g.x, a.in_vec != 0,
+                     ncomp);
+      compute_sync(ncomp);
     }
     const int lim = g.x;
     const int Te = (lim + kTileK - 1) / kTileK;
     const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
-    // ---- pass 1: tile partials of delta
-    for (int t = w; t < Te; t += nw) {
-      const int j0 = t * kTileK + lane * kLaneKeys;
-      float p[8], d[8];
-      tile_pdp<T>(sp, sd, j0, p, d);
-      const bool masked = km != nullptr || (t + 1) * kTileK > lim;
-      const float part = tile_dot(p, d, j0, lim, km, masked);
-      if (lane == 0) td[t] = part;
-    }
-
-    if (__syncthreads_or(timed_out)) {
-      if (tid == 0) {
-        raise_device_error(a.err, kDevErrTimeout);
-        for (int64_t kk = k; kk < issued_end; ++kk) {
-          if (stall && kk == 0) continue;
-          mbar_wait_bounded(smem_addr(&bars[kk % NS]), (uint32_t)((kk / NS) & 1), a.timeout_ns);
+    // ---- pass 1: tile partials of delta, two tiles at a time
+    {
+      int t = w;
+      for (; t + nw < Te; t += 2 * nw) {
+        const int t1 = t + nw;
+        const int j0 = t * kTileK + lane * kLaneKeys, j1 = t1 * kTileK + lane * kLaneKeys;
+        float p0[8], d0[8], p1[8], d1[8];
+        tile_pdp<T>(sp, sd, j0, p0, d0);
+        tile_pdp<T>(sp, sd, j1, p1, d1);
+        float a0 = lane_dot(p0, d0, j0, lim, km, km != nullptr || (t + 1) * kTileK > lim);
+        float a1 = lane_dot(p1, d1, j1, lim, km, km != nullptr || (t1 + 1) * kTileK > lim);
+        warp_sum_xor2(a0, a1);
+        if (lane == 0) {
+          td[t] = a0;
+          td[t1] = a1;
         }
       }
+      if (t < Te) {
+        const int j0 = t * kTileK + lane * kLaneKeys;
+        float p0[8], d0[8];
+        tile_pdp<T>(sp, sd, j0, p0, d0);
+        const float a0 =
+            warp_sum_xor(lane_dot(p0, d0, j0, lim, km, km != nullptr || (t + 1) * kTileK > lim));
+        if (lane == 0) td[t] = a0;
+      }
+    }
+
+    if (compute_sync_or(ncomp, timed_out)) {
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
       return;
     }
 
-    // ---- tile partials added left to right; the previous row's stage is free now
+    // ---- tile partials added left to right (one thread)
     if (tid == 0) {
-      if (a.use_bulk && defer && k >= 1 && k - 1 + NS < nmine) {
-        const int sr = (int)((k - 1) % NS);
-        issue_row<T>(a, r0 + (k - 1 + NS) * G, ring + (size_t)sr * slot, &bars[sr], &geos[sr],
-                     false);
-        issued_end = k + NS;
-      }
+      // four partials per shared-memory load (td is 16-byte aligned)
       float delta = 0.0f;
-      for (int t = 0; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
+      int t = 0;
+      for (; t + 4 <= Te; t += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(td + t);
+        delta = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(delta, v.x), v.y), v.z), v.w);
+      }
+      for (; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
       dsm[0] = delta;
       if (a.delta) a.delta[r] = delta;
     }
-    __syncthreads();
+    compute_sync(ncomp);
     const float delta = dsm[0];
 
     // ---- pass 2: dScores
@@ -209,19 +259,15 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
       tile_grad(p, d, j0, lim, km, masked, delta, v);
       store_lane8<T>(grow, j0, a.L, ovec, v);
     }
+    if (a.use_bulk) {  // done with the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
     for (int t = Te + w; t < a.T; t += nw) {
       float z[8];
 #pragma unroll
       for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
       store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
-    }
-
-    if (!defer) {
-      __syncthreads();  // single stage: everyone is done with it before it is refilled
-      if (a.use_bulk && tid == 0 && k + NS < nmine) {
-        issue_row<T>(a, r0 + (k + NS) * G, sp, &bars[s], &geos[s], false);
-        issued_end = k + NS + 1;
-      }
     }
   }
 }
@@ -239,7 +285,12 @@ const void *bwd_fn(fos_dtype dt) {
 
 size_t bwd_extra_smem(int T, int stages) {
   (void)stages;
-  return (size_t)kBarBytes + kGeoBytes + (size_t)(T + 4) * sizeof(float);
+  return (size_t)kBarBytes + kGeoBytes + (size_t)(((T + 3) & ~3) + 4) * sizeof(float);
+}
+
+int bwd_default_warps(int T) {
+  const int w = (T + 1) / 2;  // one pair of tiles per warp
+  return w < 1 ? 1 : (w > 16 ? 16 : w);
 }
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {

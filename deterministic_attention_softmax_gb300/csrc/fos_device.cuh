@@ -43,11 +43,19 @@ __device__ __forceinline__ float scale_fos(float a, float b) {
   return (a == b) ? 1.0f : exp_fos(__fsub_rn(a, b));
 }
 
-// Maximum over the 32 lanes (exact, so any tree gives the same value).
-__device__ __forceinline__ float warp_max_xor(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-  return v;
+// Maximum over the 32 lanes.  A maximum is exact, so any combining order gives the same
+// value; the single-instruction warp reduction (PTX redux.sync .max.f32, sm_100a family) is
+// used.  NaN inputs are outside the contract.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Maximum of a lane's 8 values (exact; a balanced tree for a short dependency chain).
+__device__ __forceinline__ float max8(const float (&x)[8]) {
+  return fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+               fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
 }
 
 // Sum over the 32 lanes by the xor butterfly 16, 8, 4, 2, 1.  IEEE addition is commutative,
@@ -56,6 +64,17 @@ __device__ __forceinline__ float warp_sum_xor(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
   return v;
+}
+
+// The same butterfly on two independent values, interleaved (each gets the bits above).
+__device__ __forceinline__ void warp_sum_xor2(float &a, float &b) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ya = __shfl_xor_sync(kFull, a, o);
+    const float yb = __shfl_xor_sync(kFull, b, o);
+    a = __fadd_rn(a, ya);
+    b = __fadd_rn(b, yb);
+  }
 }
 
 // ------------------------------------------------------------------ dtype traits
@@ -250,6 +269,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (global_ns() - t0 > timeout_ns) return false;
   }
   return false;
+}
+
+// Plain arrive (count 1) on an mbarrier, e.g. a consumer warp releasing a stage.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named CTA barrier 1 over the first `nthreads` threads (the compute warps), and the same
+// barrier combined with an OR of a per-thread flag.
+__device__ __forceinline__ void compute_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ bool compute_sync_or(int nthreads, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)flag), "r"(nthreads)
+      : "memory");
+  return out != 0;
 }
 
 __device__ __forceinline__ void raise_device_error(unsigned *err, unsigned code) {

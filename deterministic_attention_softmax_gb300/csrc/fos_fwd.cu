@@ -3,31 +3,35 @@
 // One CTA owns one complete row at a time ("[WS1][kernels] Add fixed-order joint-attention
 // softmax for Qwen-Image", Summary: fixed-order online softmax).  CTAs are persistent: CTA c
 // takes rows c, c + grid, c + 2*grid, ...  On the bulk-copy path every CTA keeps a ring of
-// `stages` shared-memory row buffers; thread 0 refills a buffer with a 1-D TMA bulk copy as
-// soon as the CTA is done with it (and writes that row's geometry next to it), so several
-// rows per CTA are in flight from HBM while the current one is computed.  Per row:
+// `stages` shared-memory row buffers; a producer warp refills a buffer with a 1-D TMA bulk copy
+// as soon as the compute warps release it (and writes that row's geometry next to it), so
+// several rows per CTA are in flight from HBM while the current one is computed.  Per row, in
+// the compute warps:
 //
-//   pass 1   warp w takes tiles w, w + nw, ...; per tile: lane max, xor-tree max m_t,
+//   pass 1   warp w takes tiles w, w + nw, ... in pairs; per tile: lane max, warp max m_t,
 //            e_j = exp(x_j - m_t), ascending lane sum, xor-tree sum s_t.
 //   merge    warp 0 folds the tile states left to right, from (sink_h, 1) or (-inf, 0):
 //              M_t = max(M_{t-1}, m_t)
 //              S_t = S_{t-1} * exp(M_{t-1} - M_t) + s_t * exp(m_t - M_t)
-//            (the factors are formed lane-parallel; the fold itself is sequential), then
-//            LSE = M + log S and, per tile, c_t = exp(m_t - M) / S.
+//            (the factors are formed lane-parallel; the fold itself is sequential), then,
+//            per tile, c_t = exp(m_t - M) / S, and LSE = M + log S.
 //   pass 2   P_j = e_j * c_t, rounded once to the I/O dtype, 16-byte stores.
 //
-// e_j stays in registers when every warp has at most KT tiles (the register mode, whose
-// stage is refilled right after pass 1); longer rows recompute e_j from the staged row in
-// pass 2 (same bits) and release their stage at the next row's first barrier.  Masked keys
-// (causal bound, valid length, key mask, -inf input) enter as -inf; tiles past the row's last
-// candidate key are neither read nor reduced, and their P is written as +0.
+// The two tiles of a pair are independent, so their shuffle trees and exponentials overlap;
+// by default a CTA has ceil(T/2) warps so that a row is one pair per warp.  e_j stays in
+// registers when every warp has at most KT tiles (register mode, whose stage is released right
+// after pass 1); longer rows recompute e_j from the staged row in pass 2 (same bits).  Masked
+// keys (causal bound, valid length, key mask, -inf input) enter as -inf; tiles past the row's
+// last candidate key are neither read nor reduced, and their P is written as +0.
+#include <float.h>
+
 #include "fos_device.cuh"
 #include "fos_internal.h"
 
 namespace fos {
 namespace {
 
-constexpr int kBarBytes = 128;  // up to 16 mbarriers at the start of shared memory
+constexpr int kBarBytes = 256;  // 16 "full" and 16 "empty" mbarriers at the start
 constexpr int kGeoBytes = 256;  // up to 16 per-stage row records (int4) after them
 
 __device__ __forceinline__ void mask_keys(float (&x)[8], int j0, int lim, const uint8_t *km) {
@@ -49,29 +53,51 @@ __device__ __forceinline__ void tile_keys(const unsigned char *stage, int t, int
   if (km != nullptr || (t + 1) * kTileK > lim) mask_keys(x, j0, lim, km);
 }
 
-// Pass 1 for tile t: e_j into e and (m_t, s_t) into tm/ts (lane 0).  A tile with no valid
-// key has m_t = -inf: its e_j are exp(-inf) = +0 and s_t = +0.
+// e_j = exp(x_j - m) and their ascending lane sum.  For a tile with no valid key (m = -inf)
+// the shift is -FLT_MAX instead, so every e_j is exp(-inf) = +0; otherwise it is m itself.
+__device__ __forceinline__ float tile_exp_sum(const float (&x)[8], float m, float (&e)[8]) {
+  const float mm = fmaxf(m, -FLT_MAX);
+#pragma unroll
+  for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_fos(__fsub_rn(x[q], mm));
+  float s = e[0];
+#pragma unroll
+  for (int q = 1; q < kLaneKeys; ++q) s = __fadd_rn(s, e[q]);
+  return s;
+}
+
+// Pass 1 for one tile: e_j into e, (m_t, s_t) into tm/ts (lane 0).
 template <typename T>
-__device__ __forceinline__ void tile_stats(const unsigned char *stage, int t, int lane, int lim,
-                                           const uint8_t *km, float (&e)[8], float *tm,
-                                           float *ts) {
+__device__ __forceinline__ void tile_stats1(const unsigned char *stage, int t, int lane, int lim,
+                                            const uint8_t *km, float (&e)[8], float *tm,
+                                            float *ts) {
   float x[8];
   tile_keys<T>(stage, t, lane, lim, km, x);
-  float m = x[0];
-#pragma unroll
-  for (int q = 1; q < kLaneKeys; ++q) m = fmaxf(m, x[q]);
-  m = warp_max_xor(m);
-  const float mm = (m == -INFINITY) ? 0.0f : m;
-  float s = 0.0f;
-#pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q) {
-    e[q] = exp_fos(__fsub_rn(x[q], mm));
-    s = __fadd_rn(s, e[q]);
-  }
-  s = warp_sum_xor(s);
+  const float m = warp_max(max8(x));
+  float s = warp_sum_xor(tile_exp_sum(x, m, e));
   if (lane == 0) {
     tm[t] = m;
     ts[t] = s;
+  }
+}
+
+// Pass 1 for two tiles at once (same bits as two single calls).
+template <typename T>
+__device__ __forceinline__ void tile_stats2(const unsigned char *stage, int t0, int t1, int lane,
+                                            int lim, const uint8_t *km, float (&e0)[8],
+                                            float (&e1)[8], float *tm, float *ts) {
+  float x0[8], x1[8];
+  tile_keys<T>(stage, t0, lane, lim, km, x0);
+  tile_keys<T>(stage, t1, lane, lim, km, x1);
+  const float m0 = warp_max(max8(x0));
+  const float m1 = warp_max(max8(x1));
+  float s0 = tile_exp_sum(x0, m0, e0);
+  float s1 = tile_exp_sum(x1, m1, e1);
+  warp_sum_xor2(s0, s1);
+  if (lane == 0) {
+    tm[t0] = m0;
+    ts[t0] = s0;
+    tm[t1] = m1;
+    ts[t1] = s1;
   }
 }
 
@@ -81,24 +107,31 @@ __device__ __forceinline__ void tile_exp(const unsigned char *stage, int t, int 
                                          const uint8_t *km, float m, float (&e)[8]) {
   float x[8];
   tile_keys<T>(stage, t, lane, lim, km, x);
-  const float mm = (m == -INFINITY) ? 0.0f : m;
+  (void)tile_exp_sum(x, m, e);
+}
+
+template <typename T>
+__device__ __forceinline__ void tile_store(unsigned char *prow, int t, int lane, int L, bool ovec,
+                                           const float (&e)[8], float c) {
+  float v[8];
 #pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_fos(__fsub_rn(x[q], mm));
+  for (int q = 0; q < kLaneKeys; ++q) v[q] = __fmul_rn(e[q], c);
+  store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, L, ovec, v);
 }
 
 // Copy keys [0, lim) of a row into the stage with plain loads (unaligned or forced path).
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
-                                            int lim, bool vec) {
+                                            int lim, bool vec, int nthreads) {
   constexpr int esz = Io<T>::kEsz;
   int start = 0;
   if (vec) {
     const int n16 = (lim * esz) >> 4;
-    for (int c = threadIdx.x; c < n16; c += blockDim.x)
+    for (int c = threadIdx.x; c < n16; c += nthreads)
       reinterpret_cast<uint4 *>(stage)[c] = reinterpret_cast<const uint4 *>(src)[c];
     start = (n16 << 4) / esz;
   }
-  for (int j = start + threadIdx.x; j < lim; j += blockDim.x) {
+  for (int j = start + threadIdx.x; j < lim; j += nthreads) {
     if (esz == 4)
       reinterpret_cast<uint32_t *>(stage)[j] = reinterpret_cast<const uint32_t *>(src)[j];
     else
@@ -124,20 +157,60 @@ __device__ __forceinline__ void issue_row(const FwdArgs &a, int64_t rr, unsigned
              bar_a);
 }
 
-template <typename T, int KT>
-__global__ void __maxnreg__(KT == 4 ? 80 : 128) fos_fwd_kernel(const FwdArgs a) {
+// Producer (lane 0 of the last warp): for each of the CTA's rows, wait until the compute
+// warps have released the stage (the "empty" barrier, one arrival per compute warp), write the
+// row's geometry next to it and start its bulk copy (the "full" barrier).  Issuing a copy can
+// block the issuing thread for a long time, so no compute warp ever issues one.  Before it
+// exits, the producer waits for every copy it issued, so shared memory is never released
+// under a copy in flight.
+template <typename T>
+__device__ void fwd_produce(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
+                            uint64_t *full, uint64_t *empty, int4 *geos, unsigned char *ring,
+                            bool stall) {
+  const int NS = a.stages;
+  uint32_t issued = 0, last_ph = 0;  // per stage: a copy was issued / parity of the last one
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t kk = 0; kk < nmine; ++kk) {
+    if (kk >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, a.timeout_ns)) {
+      raise_device_error(a.err, kDevErrTimeout);
+      break;
+    }
+    const bool skip = stall && kk == 0;
+    issue_row<T>(a, r0 + kk * G, ring + (size_t)s * a.stage_bytes, &full[s], &geos[s], skip);
+    if (!skip) {
+      issued |= 1u << s;
+      last_ph = (last_ph & ~(1u << s)) | (ph << s);
+    }
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  for (int t = 0; t < NS; ++t)
+    if (issued & (1u << t))
+      mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
+// kFast: the common case fixed at compile time (bulk copies, every row in registers, no mask,
+// no sink, 16-byte aligned output).  Both instances do the same arithmetic in the same order.
+template <typename T, int KT, bool kFast>
+__global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112)))
+    fos_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + 16;
   int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes);
   unsigned char *ring = smem + kBarBytes + kGeoBytes;
+  const int T4 = (a.T + 3) & ~3;  // stats arrays padded for 16-byte reads
   float *tm = reinterpret_cast<float *>(ring + (size_t)a.stages * a.stage_bytes);
-  float *ts = tm + a.T;
-  float *tc = ts + a.T;
-  float *ab = tc + a.T;  // merge factors: alpha at ab[0..31], beta at ab[32..63]
+  float *ts = tm + T4;
+  float *tc = ts + T4;
 
   const int tid = threadIdx.x;
-  const int nw = blockDim.x >> 5;
+  const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
+  const int ncomp = nw * 32;
   const int w = tid >> 5;
   const int lane = tid & 31;
   const int64_t G = gridDim.x;
@@ -145,143 +218,152 @@ __global__ void __maxnreg__(KT == 4 ? 80 : 128) fos_fwd_kernel(const FwdArgs a) 
   if (r0 >= a.rows) return;
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
-  const bool stall = a.test_stall && blockIdx.x == 0;
-  const bool reg_mode = a.T <= nw * KT;  // every row's e_j fit in registers
-  const bool defer = NS >= 2;            // outside register mode: refill one row later
-  int64_t issued_end = 0;                // rows [0, issued_end) of this CTA have been issued
+  const bool reg_mode = kFast || a.T <= nw * KT;  // every row's e_j fit in registers
+  const bool use_bulk = kFast || a.use_bulk != 0;
 
-  if (a.use_bulk) {
+  if (use_bulk) {
     if (tid == 0) {
-      for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&bars[s]), 1);
+      for (int t = 0; t < NS; ++t) {
+        mbar_init(smem_addr(&full[t]), 1);
+        mbar_init(smem_addr(&empty[t]), nw);
+      }
       fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0)
-      for (int64_t kk = 0; kk < nmine && kk < NS; ++kk)
-        issue_row<T>(a, r0 + kk * G, ring + (size_t)kk * a.stage_bytes, &bars[kk], &geos[kk],
-                     stall && kk == 0);
-    issued_end = nmine < NS ? nmine : NS;
+  }
+  if (w == nw) {
+    if (use_bulk && lane == 0)
+      fwd_produce<T>(a, r0, G, nmine, full, empty, geos, ring, a.test_stall && blockIdx.x == 0);
+    return;
   }
 
-  for (int64_t k = 0; k < nmine; ++k) {
+  // stage index and phase parity of row k, carried rather than computed
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t k = 0; k < nmine; ++k, s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
     const int64_t r = r0 + k * G;
-    const int s = a.use_bulk ? (int)(k % NS) : 0;
     unsigned char *stage = ring + (size_t)s * a.stage_bytes;
 
     bool timed_out = false;
     int4 g;
-    if (a.use_bulk) {
-      timed_out = !mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((k / NS) & 1), a.timeout_ns);
-      g = geos[s];
+    if (use_bulk) {
+      timed_out = !mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
+      g = kFast ? make_int4(a.L, 0, 0, 0) : geos[s];
     } else {
       if (tid == 0) geos[0] = row_geometry(a, r);
-      __syncthreads();  // also: every warp is done with the previous row's stage
+      compute_sync(ncomp);  // also: every warp is done with the previous row's stage
       g = geos[0];
       plain_stage<T>(stage, static_cast<const unsigned char *>(a.scores) + (size_t)r * a.ld * esz,
-                     g.x, a.in_vec != 0);
-      __syncthreads();
+                     g.x, a.in_vec != 0, ncomp);
+      compute_sync(ncomp);
     }
     const int lim = g.x;
     const int Te = (lim + kTileK - 1) / kTileK;
-    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+    const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
-    // ---- pass 1: tile statistics
+    // ---- pass 1: tile statistics, two tiles at a time
     float e[KT][8];
     if (reg_mode) {
 #pragma unroll
-      for (int kk = 0; kk < KT; ++kk) {
-        const int t = w + kk * nw;
-        if (t < Te) tile_stats<T>(stage, t, lane, lim, km, e[kk], tm, ts);
+      for (int kk = 0; kk < KT; kk += 2) {
+        const int t0 = w + kk * nw, t1 = t0 + nw;
+        if (t1 < Te)
+          tile_stats2<T>(stage, t0, t1, lane, lim, km, e[kk], e[kk + 1], tm, ts);
+        else if (t0 < Te)
+          tile_stats1<T>(stage, t0, lane, lim, km, e[kk], tm, ts);
+      }
+      if (use_bulk) {  // the stage is free: e_j are in registers
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
       }
     } else {
-      for (int t = w; t < Te; t += nw) {
-        float tmp[8];
-        tile_stats<T>(stage, t, lane, lim, km, tmp, tm, ts);
+      int t = w;
+      for (; t + nw < Te; t += 2 * nw) {
+        float e0[8], e1[8];
+        tile_stats2<T>(stage, t, t + nw, lane, lim, km, e0, e1, tm, ts);
+      }
+      if (t < Te) {
+        float e0[8];
+        tile_stats1<T>(stage, t, lane, lim, km, e0, tm, ts);
       }
     }
 
-    if (__syncthreads_or(timed_out)) {
-      // A copy never landed: record it, let the copies still in flight land, stop.
-      if (tid == 0) {
-        raise_device_error(a.err, kDevErrTimeout);
-        for (int64_t kk = k; kk < issued_end; ++kk) {
-          if (stall && kk == 0) continue;
-          mbar_wait_bounded(smem_addr(&bars[kk % NS]), (uint32_t)((kk / NS) & 1), a.timeout_ns);
-        }
-      }
+    if (compute_sync_or(ncomp, timed_out)) {
+      // A copy never landed: record it and stop (the producer drains the copies in flight).
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
       return;
     }
 
-    // Refill a free stage: this row's in register mode (pass 1 was its last reader); with
-    // two or more stages, the previous row's (its pass 2 ended before this barrier); with a
-    // single stage outside register mode, this row's after an end-of-row barrier below.
-    if (a.use_bulk && tid == 0 && (reg_mode || defer)) {
-      const int64_t kr = reg_mode ? k : k - 1;
-      if (kr >= 0 && kr + NS < nmine) {
-        const int sr = (int)(kr % NS);
-        issue_row<T>(a, r0 + (kr + NS) * G, ring + (size_t)sr * a.stage_bytes, &bars[sr],
-                     &geos[sr], false);
-        issued_end = kr + NS + 1;
-      }
-    }
-
-    // ---- merge (warp 0): ordered fold of the tile states, LSE, per-tile output scale
+    // ---- merge (warp 0)
+    float M = -INFINITY, S = 0.0f;
     if (w == 0) {
-      const bool has_sink = a.sink != nullptr;
-      float M = has_sink ? a.sink[g.z] : -INFINITY;
-      float S = has_sink ? 1.0f : 0.0f;
+      if (!kFast && a.sink != nullptr) {
+        M = a.sink[g.z];
+        S = 1.0f;
+      }
       for (int base = 0; base < Te; base += 32) {
         const int t = base + lane;
         const float mt = t < Te ? tm[t] : -INFINITY;
         const float st = t < Te ? ts[t] : 0.0f;
-        float pm = mt;  // inclusive prefix maximum inside this group of 32 tiles
+        float pm = mt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float y = __shfl_up_sync(kFull, pm, o);
           if (lane >= o) pm = fmaxf(pm, y);
         }
-        pm = fmaxf(pm, M);  // M_t
+        pm = fmaxf(pm, M);
         float prev = __shfl_up_sync(kFull, pm, 1);
-        if (lane == 0) prev = M;  // M_{t-1}
-        ab[lane] = scale_fos(prev, pm);
-        ab[32 + lane] = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_fos(mt, pm));
-        __syncwarp();
+        if (lane == 0) prev = M;
+        const float alpha = scale_fos(prev, pm);
+        const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_fos(mt, pm));
         const int n = min(32, Te - base);
-        for (int q = 0; q < n; ++q) S = __fadd_rn(__fmul_rn(S, ab[q]), ab[32 + q]);
+        for (int q0 = 0; q0 < n; q0 += 4) {
+          float av[4], bv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            av[i] = __shfl_sync(kFull, alpha, q0 + i);
+            bv[i] = __shfl_sync(kFull, beta, q0 + i);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float ns = __fadd_rn(__fmul_rn(S, av[i]), bv[i]);
+            S = (q0 + i < n) ? ns : S;
+          }
+        }
         M = __shfl_sync(kFull, pm, n - 1);
-        __syncwarp();
       }
       for (int t = lane; t < Te; t += 32) {
         const float mt = tm[t];
         tc[t] = (mt == -INFINITY) ? 0.0f : __fdiv_rn(scale_fos(mt, M), S);
       }
-      if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
     }
-    __syncthreads();
+    compute_sync(ncomp);
+    if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
     // ---- pass 2: P = e * c_t, one rounding, 16-byte stores
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
-    const bool ovec = a.out_vec != 0;
+    const bool ovec = kFast || a.out_vec != 0;
     if (reg_mode) {
 #pragma unroll
-      for (int kk = 0; kk < KT; ++kk) {
-        const int t = w + kk * nw;
-        if (t < Te) {
-          const float c = tc[t];
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < kLaneKeys; ++q) v[q] = __fmul_rn(e[kk][q], c);
-          store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, v);
+      for (int kk = 0; kk < KT; kk += 2) {
+        const int t0 = w + kk * nw, t1 = t0 + nw;
+        if (t1 < Te) {
+          const float c0 = tc[t0], c1 = tc[t1];
+          tile_store<T>(prow, t0, lane, a.L, ovec, e[kk], c0);
+          tile_store<T>(prow, t1, lane, a.L, ovec, e[kk + 1], c1);
+        } else if (t0 < Te) {
+          tile_store<T>(prow, t0, lane, a.L, ovec, e[kk], tc[t0]);
         }
       }
     } else {
       for (int t = w; t < Te; t += nw) {
-        float ee[8], v[8];
+        float ee[8];
         tile_exp<T>(stage, t, lane, lim, km, tm[t], ee);
-        const float c = tc[t];
-#pragma unroll
-        for (int q = 0; q < kLaneKeys; ++q) v[q] = __fmul_rn(ee[q], c);
-        store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, v);
+        tile_store<T>(prow, t, lane, a.L, ovec, ee, tc[t]);
+      }
+      if (use_bulk) {  // done with the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
       }
     }
     for (int t = Te + w; t < a.T; t += nw) {
@@ -291,73 +373,76 @@ __global__ void __maxnreg__(KT == 4 ? 80 : 128) fos_fwd_kernel(const FwdArgs a) 
       store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
     }
     // Tile t's tm entry is written (pass 1) and re-read (pass 2) by warp t % nw only, and tc
-    // is rewritten after the next row's first barrier, so no barrier is needed here unless a
-    // single stage must be refilled now.
-    if (!reg_mode && !defer) {
-      __syncthreads();
-      if (a.use_bulk && tid == 0 && k + NS < nmine) {
-        issue_row<T>(a, r0 + (k + NS) * G, stage, &bars[s], &geos[s], false);
-        issued_end = k + NS + 1;
-      }
-    }
+    // is rewritten after the next row's first barrier: no barrier is needed here.
   }
 }
 
-template <int KT>
-const void *fwd_fn(fos_dtype dt) {
+template <int KT, bool kFast>
+const void *fwd_fn_kt(fos_dtype dt) {
   switch (dt) {
-    case FOS_F32: return reinterpret_cast<const void *>(&fos_fwd_kernel<float, KT>);
-    case FOS_BF16: return reinterpret_cast<const void *>(&fos_fwd_kernel<__nv_bfloat16, KT>);
-    case FOS_F16: return reinterpret_cast<const void *>(&fos_fwd_kernel<__half, KT>);
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_fwd_kernel<float, KT, kFast>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_fwd_kernel<__nv_bfloat16, KT, kFast>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_fwd_kernel<__half, KT, kFast>);
   }
   return nullptr;
 }
 
-const void *fwd_fn(fos_dtype dt, int kt) { return kt <= 4 ? fwd_fn<4>(dt) : fwd_fn<8>(dt); }
+template <bool kFast>
+const void *fwd_fn_f(fos_dtype dt, int kt) {
+  switch (kt) {
+    case 2: return fwd_fn_kt<2, kFast>(dt);
+    case 4: return fwd_fn_kt<4, kFast>(dt);
+    case 6: return fwd_fn_kt<6, kFast>(dt);
+    default: return fwd_fn_kt<8, kFast>(dt);
+  }
+}
 
-template <typename T, int KT>
-void launch_t(const FwdArgs &a, int grid, int threads, size_t smem, cudaStream_t s) {
-  fos_fwd_kernel<T, KT><<<grid, threads, smem, s>>>(a);
+const void *fwd_fn(fos_dtype dt, int kt, bool fast) {
+  return fast ? fwd_fn_f<true>(dt, kt) : fwd_fn_f<false>(dt, kt);
 }
 
 }  // namespace
 
 size_t fwd_extra_smem(int T, int stages) {
   (void)stages;
-  return (size_t)kBarBytes + kGeoBytes + (size_t)(3 * T + 64) * sizeof(float);
+  return (size_t)kBarBytes + kGeoBytes + (size_t)3 * ((T + 3) & ~3) * sizeof(float);
 }
 
 int fwd_tiles_per_warp(int T, int warps) {
-  // 4 tiles per warp when they fit, else 8; beyond 8 per warp e_j are recomputed.
-  return (T <= 4 * warps) ? 4 : 8;
+  // the smallest even count of 2..8 that holds the row; past 8 per warp e_j are recomputed
+  const int need = (T + warps - 1) / warps;
+  if (need <= 2) return 2;
+  if (need <= 4) return 4;
+  if (need <= 6) return 6;
+  return 8;
+}
+
+int fwd_default_warps(int T) {
+  const int w = (T + 5) / 6;  // up to six tiles (three pairs) per warp
+  return w < 1 ? 1 : (w > 16 ? 16 : w);
 }
 
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
-  for (int kt : {4, 8}) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fwd_fn(dt, kt), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return e;
-  }
+  for (int kt : {2, 4, 6, 8})
+    for (bool fast : {false, true}) {
+      cudaError_t e = cudaFuncSetAttribute(fwd_fn(dt, kt, fast),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
-cudaError_t fwd_occupancy(fos_dtype dt, int kt, int threads, size_t smem, int *blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_fn(dt, kt), threads,
-                                                       smem);
+cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,
+                          int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_fn(dt, kt, fast),
+                                                       threads, smem);
 }
 
-cudaError_t fwd_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
+cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s) {
-  const bool k4 = kt <= 4;
-  switch (dt) {
-    case FOS_F32: k4 ? launch_t<float, 4>(a, grid, threads, smem, s)
-                     : launch_t<float, 8>(a, grid, threads, smem, s); break;
-    case FOS_BF16: k4 ? launch_t<__nv_bfloat16, 4>(a, grid, threads, smem, s)
-                      : launch_t<__nv_bfloat16, 8>(a, grid, threads, smem, s); break;
-    case FOS_F16: k4 ? launch_t<__half, 4>(a, grid, threads, smem, s)
-                     : launch_t<__half, 8>(a, grid, threads, smem, s); break;
-  }
-  return cudaGetLastError();
+  const void *fn = fwd_fn(dt, kt, fast);
+  void *args[] = {const_cast<FwdArgs *>(&a)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, smem, s);
 }
 
 }  // namespace fos

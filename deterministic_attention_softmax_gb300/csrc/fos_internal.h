@@ -59,11 +59,16 @@ size_t fwd_extra_smem(int T, int stages);
 size_t bwd_extra_smem(int T, int stages);
 
 // Kernel instances per dtype: set the dynamic shared-memory limit, query residency, launch.
-// The forward keeps e_j of `kt` tiles per warp in registers (kt = 4 or 8).
+// The forward keeps e_j of `kt` tiles per warp in registers (kt = 2, 4, 6 or 8); `fast`
+// selects the instance specialised for the common case (same arithmetic).
 int fwd_tiles_per_warp(int T, int warps);
+// Default compute warps per CTA (1..16).
+int fwd_default_warps(int T);
+int bwd_default_warps(int T);
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
-cudaError_t fwd_occupancy(fos_dtype dt, int kt, int threads, size_t smem, int *blocks_per_sm);
-cudaError_t fwd_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
+cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,
+                          int *blocks_per_sm);
+cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem);

@@ -106,7 +106,7 @@ typedef struct fos_launch {
   int32_t load_path;     /* 0 = auto, 1 = bulk copy (TMA) only, 2 = plain loads only */
   int64_t wait_timeout_ns; /* 0 = default (2 s): limit of every bounded wait in a kernel */
   int32_t test_stall;    /* 0; 1 = CTA 0 waits on a copy that is never issued (test only) */
-  int32_t reserved;      /* must be 0 */
+  int32_t generic;       /* 0 = auto; 1 = never the kernel specialised for the common case */
 } fos_launch;
 
 /*

@@ -93,11 +93,11 @@ def test_rejects_null_pointers_and_bad_dtype(abi):
 
 @pytest.mark.parametrize("bad", [
     dict(warps_per_cta=17), dict(warps_per_cta=-1), dict(ctas=-2), dict(stages=17),
-    dict(load_path=3), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(reserved=1),
+    dict(load_path=3), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(generic=2),
 ])
 def test_rejects_bad_launch_options(abi, bad):
     opts = dict(warps_per_cta=0, ctas=0, stages=0, load_path=0, wait_timeout_ns=0, test_stall=0,
-                reserved=0)
+                generic=0)
     opts.update(bad)
     lc = abi.FosLaunch(**opts)
     d = _desc(abi)

@@ -108,6 +108,29 @@ def test_launch_geometry(dtype_name, opts):
         assert bits_equal(a, b_)
 
 
+UNMASKED_LAUNCHES = [
+    dict(generic=1), dict(warps_per_cta=1), dict(warps_per_cta=2), dict(warps_per_cta=3),
+    dict(warps_per_cta=5), dict(warps_per_cta=9), dict(warps_per_cta=16), dict(ctas=7),
+    dict(stages=1), dict(stages=2), dict(load_path=2), dict(generic=1, warps_per_cta=3),
+]
+
+
+@pytest.mark.parametrize("dtype_name", ["bfloat16", "float32", "float16"])
+@pytest.mark.parametrize("L", [4352, 4400, 8192])
+@pytest.mark.parametrize("opts", UNMASKED_LAUNCHES,
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
+def test_unmasked_rows_fast_and_generic_kernels_agree(dtype_name, L, opts):
+    # Unmasked, sink-free, aligned rows take the kernel specialised for that case by default;
+    # every other launch (generic kernel, plain loads, other register splits) gives its bits.
+    dt = DTYPES[dtype_name]
+    x = W.normal((300, L), 4.0, 41, dt, dev())
+    dp = W.normal((300, L), 1.0, 42, dt, dev())
+    ref = fwd_bwd(x, dp)
+    out = fwd_bwd(x, dp, launch=fos.Launch(**opts))
+    for a, b_ in zip(ref, out):
+        assert bits_equal(a, b_)
+
+
 @pytest.mark.parametrize("dtype_name", ["bfloat16", "float32", "float16"])
 def test_unaligned_copy_matches_aligned(dtype_name):
     # same rows at a base pointer one element off 16-byte alignment (plain element loads and
