@@ -242,16 +242,24 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
   BwdArgs a{};
   Plan pl;
   const void *inputs[2] = {probs, dprobs};
+  const int esz = dtype_size(dtype);
+  const bool fast = !(launch && launch->generic) && !(launch && launch->load_path == 2) &&
+                    !desc->causal && !desc->kv_valid_len && !desc->key_mask &&
+                    aligned16(probs) && aligned16(dprobs) && aligned16(dscores) &&
+                    ((desc->ld * esz) & 15) == 0 && (((int64_t)desc->key_len * esz) & 15) == 0;
   st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
                  bwd_default_warps((desc->key_len + kTileK - 1) / kTileK),
-                 [dtype](int th, size_t sm, int *n) { return bwd_occupancy(dtype, th, sm, n); },
+                 [dtype, fast](int th, size_t sm, int *n) {
+                   return bwd_occupancy(dtype, fast, th, sm, n);
+                 },
                  &a, &pl);
   if (st != FOS_OK) return st;
   a.probs = probs;
   a.dprobs = dprobs;
   a.dscores = dscores;
   a.delta = delta;
-  if (bwd_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+  if (bwd_launch(dtype, fast && a.use_bulk && a.out_vec, a, pl.grid, pl.threads, pl.smem,
+                 stream) != cudaSuccess)
     return FOS_ERR_CUDA;
   return FOS_OK;
 }

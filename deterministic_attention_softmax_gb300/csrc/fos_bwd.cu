@@ -132,7 +132,9 @@ __device__ void bwd_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmi
       mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
 }
 
-template <typename T>
+// kFast: the common case fixed at compile time (bulk copies, no mask, 16-byte aligned output).
+// Both instances do the same arithmetic in the same order.
+template <typename T, bool kFast>
 __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
@@ -154,8 +156,9 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   if (r0 >= a.rows) return;
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
+  const bool use_bulk = kFast || a.use_bulk != 0;
 
-  if (a.use_bulk) {
+  if (use_bulk) {
     if (tid == 0) {
       for (int t = 0; t < NS; ++t) {
         mbar_init(smem_addr(&full[t]), 1);
@@ -166,7 +169,7 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
     __syncthreads();
   }
   if (w == nw) {
-    if (a.use_bulk && lane == 0)
+    if (use_bulk && lane == 0)
       bwd_produce<T>(a, r0, G, nmine, full, empty, geos, ring, slot,
                      a.test_stall && blockIdx.x == 0);
     return;
@@ -182,9 +185,9 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
 
     bool timed_out = false;
     int4 g;
-    if (a.use_bulk) {
+    if (use_bulk) {
       timed_out = !mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
-      g = geos[s];
+      g = kFast ? make_int4(a.L, 0, 0, 0) : geos[s];
     } else {
       if (tid == 0) geos[0] = row_geometry(a, r);
       compute_sync(ncomp);  // also: every warp is done with the previous row's stage
@@ -198,7 +201,7 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
     }
     const int lim = g.x;
     const int Te = (lim + kTileK - 1) / kTileK;
-    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+    const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: tile partials of delta, two tiles at a time
     {
@@ -250,7 +253,7 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
 
     // ---- pass 2: dScores
     unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
-    const bool ovec = a.out_vec != 0;
+    const bool ovec = kFast || a.out_vec != 0;
     for (int t = w; t < Te; t += nw) {
       const int j0 = t * kTileK + lane * kLaneKeys;
       float p[8], d[8], v[8];
@@ -259,7 +262,7 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
       tile_grad(p, d, j0, lim, km, masked, delta, v);
       store_lane8<T>(grow, j0, a.L, ovec, v);
     }
-    if (a.use_bulk) {  // done with the stage
+    if (use_bulk) {  // done with the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
     }
@@ -272,14 +275,17 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
   }
 }
 
-const void *bwd_fn(fos_dtype dt) {
+template <bool kFast>
+const void *bwd_fn_f(fos_dtype dt) {
   switch (dt) {
-    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_kernel<float>);
-    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__nv_bfloat16>);
-    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__half>);
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_kernel<float, kFast>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__nv_bfloat16, kFast>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__half, kFast>);
   }
   return nullptr;
 }
+
+const void *bwd_fn(fos_dtype dt, bool fast) { return fast ? bwd_fn_f<true>(dt) : bwd_fn_f<false>(dt); }
 
 }  // namespace
 
@@ -289,26 +295,28 @@ size_t bwd_extra_smem(int T, int stages) {
 }
 
 int bwd_default_warps(int T) {
-  const int w = (T + 1) / 2;  // one pair of tiles per warp
+  const int w = (T + 3) / 4;  // about four tiles per warp
   return w < 1 ? 1 : (w > 16 ? 16 : w);
 }
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {
-  return cudaFuncSetAttribute(bwd_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-}
-
-cudaError_t bwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, bwd_fn(dt), threads, smem);
-}
-
-cudaError_t bwd_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
-                       cudaStream_t s) {
-  switch (dt) {
-    case FOS_F32: fos_bwd_kernel<float><<<grid, threads, smem, s>>>(a); break;
-    case FOS_BF16: fos_bwd_kernel<__nv_bfloat16><<<grid, threads, smem, s>>>(a); break;
-    case FOS_F16: fos_bwd_kernel<__half><<<grid, threads, smem, s>>>(a); break;
+  for (bool fast : {false, true}) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_fn(dt, fast),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
+}
+
+cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, bwd_fn(dt, fast), threads,
+                                                       smem);
+}
+
+cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
+                       size_t smem, cudaStream_t s) {
+  void *args[] = {const_cast<BwdArgs *>(&a)};
+  return cudaLaunchKernel(bwd_fn(dt, fast), dim3(grid), dim3(threads), args, smem, s);
 }
 
 }  // namespace fos

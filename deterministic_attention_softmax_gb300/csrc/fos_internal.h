@@ -72,9 +72,9 @@ cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int gr
                        size_t smem, cudaStream_t s);
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
-cudaError_t bwd_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
-cudaError_t bwd_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
-                       cudaStream_t s);
+cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
+                       size_t smem, cudaStream_t s);
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
 
