@@ -1,0 +1,75 @@
+"""The benchmark's multi-rank host logic on the CPU (world size 2, gloo): barrier, max and sum
+over ranks, and the reference arm running on rank 0 only.  Rows are independent, so ranks run
+replicas with no data-path exchange; this covers the timing and aggregation around them."""
+
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(dist)
+        mx = bench.max_over_ranks(dist, 1.5 + rank, "cpu")   # per-rank ms per step
+        sm = bench.sum_over_ranks(dist, 100.0 * (rank + 1), "cpu")  # per-rank bytes
+        out.put((rank, mx, sm))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_and_sum_over_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.5, 2.5]      # the slowest rank's time, on every rank
+    assert [r[2] for r in res] == [300.0, 300.0]  # all ranks' bytes
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    # a non-zero rank of a torchrun launch exits 0 without work and prints nothing
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0
+    assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_one_line_on_a_single_rank():
+    import json
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
