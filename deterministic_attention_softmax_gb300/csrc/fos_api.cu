@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kBarBytes = 128;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultWarps = 8;
-constexpr size_t kStageTarget = 48 * 1024;  // ring bytes per CTA aimed at by default
+
 constexpr int kMaxStages = 16;
 
 struct DevInfo {
@@ -110,8 +110,8 @@ struct Plan {
 template <typename OccFn>
 fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
-                     size_t (*extra)(int, int), int default_warps, OccFn occ, RowArgs *ra,
-                     Plan *pl) {
+                     size_t (*extra)(int, int), int default_warps, size_t stage_target,
+                     OccFn occ, RowArgs *ra, Plan *pl) {
   const int esz = dtype_size(dt);
   const int T = (d->key_len + kTileK - 1) / kTileK;
   const size_t stage_bytes = (size_t)T * kTileK * esz;
@@ -132,7 +132,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
     if (l && l->stages) {
       stages = l->stages;
     } else {
-      stages = (int)(kStageTarget / slot);
+      stages = (int)(stage_target / slot);
       stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     }
     while (stages > 1 && fixed + stages * slot > (size_t)dev.max_smem) --stages;
@@ -210,7 +210,8 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask && !desc->sink &&
                     aligned16(scores) && aligned16(probs) && ((desc->ld * esz) & 15) == 0 &&
                     (((int64_t)desc->key_len * esz) & 15) == 0;
-  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem, warps,
+  // ring of about 24 KB per CTA: rows are consumed right after their tile pass
+  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem, warps, 24 * 1024,
                  [dtype, kt, fast](int th, size_t sm, int *n) {
                    return fwd_occupancy(dtype, kt, fast, th, sm, n);
                  },
@@ -248,7 +249,7 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
                     aligned16(probs) && aligned16(dprobs) && aligned16(dscores) &&
                     ((desc->ld * esz) & 15) == 0 && (((int64_t)desc->key_len * esz) & 15) == 0;
   st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
-                 bwd_default_warps((desc->key_len + kTileK - 1) / kTileK),
+                 bwd_default_warps((desc->key_len + kTileK - 1) / kTileK), 48 * 1024,
                  [dtype, fast](int th, size_t sm, int *n) {
                    return bwd_occupancy(dtype, fast, th, sm, n);
                  },

@@ -43,6 +43,24 @@ __device__ __forceinline__ float scale_fos(float a, float b) {
   return (a == b) ? 1.0f : exp_fos(__fsub_rn(a, b));
 }
 
+// The same exponential with results below 2^-126 flushed to zero (PTX ex2.approx.ftz.f32): one
+// instruction instead of the subnormal-keeping sequence.  For arguments whose result is at least
+// 2^-126 it returns the same bits as exp_fos.  Used only where a flushed value provably cannot
+// change a result: when no key of a tile lies more than 87 below the tile maximum
+// (87 * log2 e < 126), and for the merge's rescale factors, whose subnormal values are always
+// added to a term of at least 1 (the tile or sink holding the running maximum contributes
+// exp(0) = 1), far below half an ulp of it.
+__device__ __forceinline__ float exp_ftz(float d) {
+  const float t = __fmul_rn(d, 1.44269504088896340736f);
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+__device__ __forceinline__ float scale_ftz(float a, float b) {
+  return (a == b) ? 1.0f : exp_ftz(__fsub_rn(a, b));
+}
+
 // Maximum over the 32 lanes.  A maximum is exact, so any combining order gives the same
 // value; the single-instruction warp reduction (PTX redux.sync .max.f32, sm_100a family) is
 // used.  NaN inputs are outside the contract.
@@ -52,10 +70,26 @@ __device__ __forceinline__ float warp_max(float v) {
   return r;
 }
 
-// Maximum of a lane's 8 values (exact; a balanced tree for a short dependency chain).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum / minimum of a lane's 8 values (exact, so the grouping does not matter; three-input
+// min/max instructions of the sm_100 family).
 __device__ __forceinline__ float max8(const float (&x)[8]) {
-  return fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-               fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  return max3f(max3f(x[0], x[1], x[2]), max3f(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+}
+
+__device__ __forceinline__ float min8(const float (&x)[8]) {
+  return min3f(min3f(x[0], x[1], x[2]), min3f(x[3], x[4], x[5]), fminf(x[6], x[7]));
 }
 
 // Sum over the 32 lanes by the xor butterfly 16, 8, 4, 2, 1.  IEEE addition is commutative,

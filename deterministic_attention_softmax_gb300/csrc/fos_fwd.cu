@@ -55,10 +55,18 @@ __device__ __forceinline__ void tile_keys(const unsigned char *stage, int t, int
 
 // e_j = exp(x_j - m) and their ascending lane sum.  For a tile with no valid key (m = -inf)
 // the shift is -FLT_MAX instead, so every e_j is exp(-inf) = +0; otherwise it is m itself.
+// Unless some key of the tile lies more than 87 below the maximum (a warp-uniform test), no
+// e_j can be below 2^-126 and the flush-to-zero exponential gives the same bits.
 __device__ __forceinline__ float tile_exp_sum(const float (&x)[8], float m, float (&e)[8]) {
   const float mm = fmaxf(m, -FLT_MAX);
+  const bool deep = __any_sync(kFull, __fsub_rn(min8(x), mm) < -87.0f);
+  if (!deep) {
 #pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_fos(__fsub_rn(x[q], mm));
+    for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_ftz(__fsub_rn(x[q], mm));
+  } else {
+#pragma unroll
+    for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_fos(__fsub_rn(x[q], mm));
+  }
   float s = e[0];
 #pragma unroll
   for (int q = 1; q < kLaneKeys; ++q) s = __fadd_rn(s, e[q]);
@@ -314,8 +322,9 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
         pm = fmaxf(pm, M);
         float prev = __shfl_up_sync(kFull, pm, 1);
         if (lane == 0) prev = M;
-        const float alpha = scale_fos(prev, pm);
-        const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_fos(mt, pm));
+        // flushing these factors cannot change S (see scale_ftz)
+        const float alpha = scale_ftz(prev, pm);
+        const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
         const int n = min(32, Te - base);
         for (int q0 = 0; q0 < n; q0 += 4) {
           float av[4], bv[4];

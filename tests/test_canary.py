@@ -77,6 +77,6 @@ def test_outputs_stay_inside_their_rows(dtype_name, L, ld, masked):
     assert torch.isfinite(lse).all() or masked
     if sink is not None:
         sb, d_sink = guarded_vec(H, 0x3C)
-        fos.fos_sink_grad(lse, delta, sink, d_sink, **kw)
+        fos.fos_sink_grad(lse, delta, sink, d_sink, batch=B, heads=H, q_len=Sq)
         torch.cuda.synchronize()
         assert vec_untouched(sb, H, 0x3C), "sink gradient wrote outside d_sink"

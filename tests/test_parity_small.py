@@ -183,3 +183,27 @@ def test_exp_accuracy_on_two_key_rows():
     p1_ref = e / (1 + e)
     err = np.abs(np64(p)[:, 1] - p1_ref)
     assert err.max() < 2e-7, err.max()
+
+
+@pytest.mark.parametrize("dtype_name", list(DTYPES))
+def test_deep_tiles_keep_subnormal_results(dtype_name):
+    # One dominant key per row (x = 0) and every other key 88..94 below it: the normaliser is
+    # about 1, so those probabilities are about e^-88..e^-94, below 2^-126 (subnormal in float32
+    # and bf16, where 1 ULP of the FP64 value is 2^-133).  The dominant key's tile holds keys
+    # more than 87 below its maximum and must keep subnormal exponentials; the other tiles
+    # reach the subnormal range through their per-tile scale.
+    dt = DTYPES[dtype_name]
+    g = torch.Generator(device="cuda").manual_seed(77)
+    rows, L = 40, 2048
+    x = -88.0 - 6.0 * torch.rand(rows, L, generator=g, device=dev())
+    x[:, 0] = 0.0
+    x = x.to(dt)
+    p, lse = fos.fos_softmax_fwd(x, q_len=rows)
+    p_ref, lse_ref = oracle.softmax_fwd(np64(x), batch=1, heads=1, q_len=rows)
+    check_fwd(p, lse, p_ref, lse_ref, dtype_name, "deep tiles")
+    if dtype_name != "float16":  # fp16 has no range down there
+        tiny = (p_ref > 2.0 ** -133) & (p_ref < 2.0 ** -126)
+        assert tiny.sum() > 1000 and (np64(p)[tiny] > 0).all()
+        first_tile = np.zeros_like(tiny)
+        first_tile[:, 1:256] = True
+        assert (tiny & first_tile).any()  # the exact path of the dominant key's tile
