@@ -298,6 +298,14 @@ def run_ours(args):
     dt = {torch.float32: _abi.FOS_F32, torch.bfloat16: _abi.FOS_BF16,
           torch.float16: _abi.FOS_F16}[w.dtype]
 
+    # ---- masks and sink of the workload (valid lengths are given to both passes, so padded
+    # keys are neither read nor reduced)
+    kv = W.valid_lengths(w)
+    kv = None if kv is None else kv.to(dev)
+    sink = W.sink_logits(w)
+    sink = None if sink is None else sink.to(dev)
+    geo = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal, kv_valid_len=kv)
+
     # ---- inputs, resident in HBM: N_SETS rotating sets (rank-distinct seeds)
     sets = []
     for s in range(N_SETS):
@@ -316,14 +324,19 @@ def run_ours(args):
     from oracle import tolerance as tol
 
     s0 = sets[0]
-    fos.fos_softmax_fwd(s0["x"], s0["p"], s0["lse"], q_len=w.rows)
+    fos.fos_softmax_fwd(s0["x"], s0["p"], s0["lse"], sink=sink, **geo)
     ids = np.unique(np.concatenate([[0, w.rows - 1], np.random.default_rng(0).integers(0, w.rows, 30)]))
     ids_d = torch.from_numpy(ids).to(dev)
     xs = s0["x"].index_select(0, ids_d).double().cpu().numpy()
-    p_ref, lse_ref = oracle.softmax_fwd(xs, batch=1, heads=1, q_len=w.rows, row_ids=ids)
+    okw = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal,
+               kv_valid_len=None if kv is None else kv.cpu().numpy(), row_ids=ids)
+    p_ref, lse_ref = oracle.softmax_fwd(xs, sink=None if sink is None else sink.double().cpu().numpy(),
+                                        **okw)
     dname = str(w.dtype).replace("torch.", "")
     ok_p = tol.check_probs(s0["p"].index_select(0, ids_d).double().cpu().numpy(), p_ref, dname)[0]
     ok_l = tol.check_lse(s0["lse"].index_select(0, ids_d).double().cpu().numpy(), lse_ref)[0]
+    # backward gate on the sampled rows alone (as rows of one head, no mask: their P is 0 on
+    # masked keys already)
     p_in = torch.from_numpy(p_ref).to(w.dtype).to(dev)
     dps = s0["dp"].index_select(0, ids_d).contiguous()
     ds_s, delta_s = fos.fos_softmax_bwd(p_in, dps, q_len=len(ids))
@@ -335,7 +348,10 @@ def run_ours(args):
         raise SystemExit(f"parity gate failed before timing: P {ok_p} LSE {ok_l} dS {ok_d}")
 
     # ---- launch arguments prebuilt once (the timed loop is two C calls per step)
-    desc = _abi.FosDesc(w.rows, w.key_len, w.key_len, 1, 1, w.rows, 0, 0, None, None, None)
+    kvp = None if kv is None else kv.data_ptr()
+    skp = None if sink is None else sink.data_ptr()
+    desc = _abi.FosDesc(w.rows, w.key_len, w.key_len, w.batch, w.heads, w.q_len, int(w.causal), 0,
+                        kvp, None, skp)
     dref = ctypes.byref(desc)
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -344,7 +360,11 @@ def run_ours(args):
     bargs = [(dref, dt, ctypes.c_void_p(s["p"].data_ptr()), ctypes.c_void_p(s["dp"].data_ptr()),
               ctypes.c_void_p(s["ds"].data_ptr()), ctypes.c_void_p(s["delta"].data_ptr()), sh,
               None) for s in sets]
-    fwd, bwd = lib.fos_softmax_fwd, lib.fos_softmax_bwd
+    d_sink = torch.empty(w.heads, dtype=torch.float32, device=dev)
+    sargs = [(dref, ctypes.c_void_p(s["lse"].data_ptr()), ctypes.c_void_p(s["delta"].data_ptr()),
+              ctypes.c_void_p(d_sink.data_ptr()), sh, None) for s in sets]
+    fwd, bwd, sgrad = lib.fos_softmax_fwd, lib.fos_softmax_bwd, lib.fos_sink_grad
+    n_launch = 3 if sink is not None else 2
 
     def step(i, ev=None):
         k = i % N_SETS
@@ -356,6 +376,10 @@ def run_ours(args):
         st |= bwd(*bargs[k])
         if ev is not None:
             ev[2].record(stream)
+        if sink is not None:
+            st |= sgrad(*sargs[k])
+            if ev is not None:
+                ev[3].record(stream)
         if st:
             raise SystemExit(f"library call failed with status {st}")
 
@@ -364,7 +388,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(pg)
     torch.cuda.synchronize()
@@ -378,12 +402,14 @@ def run_ours(args):
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    sink_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) if sink is not None else 0.0
     assert fos.fos_device_error() == 0
     ms_step_rank = total_ms / K
     ms_step = max_over_ranks(pg, ms_step_rank, dev)
 
-    b = W.algorithmic_bytes(w)
-    step_bytes = b["fwd"] + b["bwd"]
+    vk = W.mean_valid_keys(w)
+    b = W.algorithmic_bytes(w, valid_keys=vk)
+    step_bytes = b["fwd"] + b["bwd"] + b["sink"]
     total_bytes = sum_over_ranks(pg, step_bytes, dev)
     value = total_bytes / (ms_step * 1e-3) / 1e9
     fwd_gbs = b["fwd"] / (fwd_ms * 1e-3) / 1e9
@@ -410,8 +436,10 @@ def run_ours(args):
         def e2e_step():
             dx.copy_(hx, non_blocking=True)
             ddp.copy_(hdp, non_blocking=True)
-            p, lse = fos.fos_softmax_fwd(dx, q_len=w.rows)
-            ds, delta = fos.fos_softmax_bwd(p, ddp, q_len=w.rows)
+            p, lse = fos.fos_softmax_fwd(dx, sink=sink, **geo)
+            ds, delta = fos.fos_softmax_bwd(p, ddp, **geo)
+            if sink is not None:
+                fos.fos_sink_grad(lse, delta, sink, batch=w.batch, heads=w.heads, q_len=w.q_len)
             hp.copy_(p, non_blocking=True)
             hds.copy_(ds, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
@@ -450,18 +478,21 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else str(w.dtype).replace("torch.", ""),
+        "scaling": "weak", "vs_baseline": None, "dtype": {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16"}[w.dtype],
         "data": "synthetic",
-        "config": {"workload": w.name, "rows": w.rows, "key_len": w.key_len,
-                   "parallelism": f"replicas x{world} (rows of each rank independent)",
-                   "l2": f"inputs larger than L2: {N_SETS} rotating input sets of "
-                         f"{set_bytes / 1e9:.2f} GB each (L2 129 MB)",
-                   "step": "fos_softmax_fwd + fos_softmax_bwd"},
+        "config": dict(w.describe(),
+                       parallelism=f"replicas x{world} (rows of each rank independent)",
+                       l2=f"inputs larger than L2: {N_SETS} rotating input sets of "
+                          f"{set_bytes / 1e9:.2f} GB each (L2 129 MB)",
+                       step="fos_softmax_fwd + fos_softmax_bwd" +
+                            (" + fos_sink_grad" if sink is not None else ""),
+                       mean_valid_keys=vk),
         "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "sink_ms": sink_ms if sink is not None else None,
         "fwd_bwd_frac_of_peak": value / world / peak,
         "rows_per_s_fwd": w.rows / (fwd_ms * 1e-3) * world,
         "rows_per_s_fwd_bwd": w.rows / (ms_step * 1e-3) * world,
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch * K,
         "clocks": clocks, "parity_gate": "sampled rows vs FP64 oracle: pass",
     }
     print(json.dumps(line))

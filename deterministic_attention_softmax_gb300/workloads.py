@@ -123,6 +123,19 @@ def sample_rows(heads: int, q_len: int, key_len: int, sigma: float, seed: int, s
     return normal((heads * q_len, key_len), sigma, seed * 100003 + sample, dtype, device)
 
 
+def mean_valid_keys(w: Workload) -> float:
+    """Mean number of keys per row that can be valid under the workload's causal bound and
+    valid lengths (the keys the kernels read)."""
+    L, Sq = w.key_len, w.q_len
+    v = float(L)
+    if w.causal:
+        v = L - Sq + (Sq + 1) / 2.0  # query i sees L - Sq + i + 1 keys
+    lens = valid_lengths(w)
+    if lens is not None:
+        v = min(v, float(lens.double().mean()))
+    return v
+
+
 def algorithmic_bytes(w: Workload, *, valid_keys: float | None = None) -> dict:
     """Bytes the method must move per pass (valid-key reads, full-row writes, FP32 per-row
     outputs): fwd = esz*|V| + esz*L + 4, bwd = 2*esz*|V| + esz*L + 4 (+4 with a sink: the
