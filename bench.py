@@ -510,10 +510,10 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     fos.build()
     w = W.WORKLOADS[args.workload]
-    geo = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal)
-    sink = None if not w.sink else W.sink_logits(w).to(dev)
     kv = W.valid_lengths(w)
     kv = None if kv is None else kv.to(dev)
+    geo = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal, kv_valid_len=kv)
+    sink = None if not w.sink else W.sink_logits(w).to(dev)
     x = W.scores(w, dev)
     p = torch.empty_like(x)
     lse = torch.empty(w.rows, dtype=torch.float32, device=dev)
@@ -522,13 +522,13 @@ def run_profile(args):
     delta = torch.empty(w.rows, dtype=torch.float32, device=dev)
     d_sink = torch.empty(w.heads, dtype=torch.float32, device=dev)
     fos.fos_softmax_fwd(x, p, lse, sink=sink, **geo)
-    fos.fos_softmax_bwd(p, dp, ds, delta, kv_valid_len=kv, **geo)
+    fos.fos_softmax_bwd(p, dp, ds, delta, **geo)
     torch.cuda.synchronize()
     for _ in range(args.warmup + args.steps):
         if args.profile == "fwd":
             fos.fos_softmax_fwd(x, p, lse, sink=sink, **geo)
         elif args.profile == "bwd":
-            fos.fos_softmax_bwd(p, dp, ds, delta, kv_valid_len=kv, **geo)
+            fos.fos_softmax_bwd(p, dp, ds, delta, **geo)
         else:
             fos.fos_sink_grad(lse, delta, sink, d_sink, batch=w.batch, heads=w.heads,
                               q_len=w.q_len)

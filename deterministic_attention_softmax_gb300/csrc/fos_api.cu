@@ -6,7 +6,9 @@
 #include <limits.h>
 #include <stdint.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "fos_internal.h"
 
@@ -26,6 +28,7 @@ constexpr int kMaxStages = 16;
 
 struct DevInfo {
   bool ready = false;
+  int index = 0;
   int sms = 0;
   int max_smem = 0;  // opt-in dynamic shared memory per block
   unsigned *err = nullptr;
@@ -41,6 +44,7 @@ fos_status device_info(DevInfo **out) {
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo &d = g_dev[dev];
   if (!d.ready) {
+    d.index = dev;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
@@ -96,6 +100,32 @@ fos_status check_launch(const fos_launch *l) {
   return FOS_OK;
 }
 
+// Resident CTAs per SM of a kernel instance at a block size and dynamic shared memory,
+// memoised: a launch asks for up to eight ring depths and the answer never changes.
+// `key` names the instance (kernel, dtype, tiles per warp, specialisation).
+template <typename OccFn>
+cudaError_t resident_ctas(int dev_index, uint32_t key, int threads, size_t smem, OccFn occ,
+                          int *per_sm) {
+  using Key = std::tuple<int, uint32_t, int, size_t>;
+  static std::map<Key, int> memo;
+  static std::mutex mu;
+  const Key k{dev_index, key, threads, smem};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find(k);
+    if (it != memo.end()) {
+      *per_sm = it->second;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = occ(threads, smem, per_sm);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (memo.size() >= 4096) memo.clear();
+  memo[k] = *per_sm;
+  return cudaSuccess;
+}
+
 // Geometry of a row-kernel launch.
 struct Plan {
   int threads = 0;
@@ -111,7 +141,7 @@ template <typename OccFn>
 fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
                      size_t (*extra)(int, int), int default_warps, size_t stage_target,
-                     OccFn occ, RowArgs *ra, Plan *pl) {
+                     uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl) {
   const int esz = dtype_size(dt);
   const int T = (d->key_len + kTileK - 1) / kTileK;
   const size_t stage_bytes = (size_t)T * kTileK * esz;
@@ -124,19 +154,38 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   const bool bulk = (path == 1) || (path == 0 && bulk_ok);
 
   const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : default_warps;
+  const int threads = (warps + 1) * 32;  // the compute warps and one producer warp
   const size_t slot = (size_t)copies * stage_bytes;
   const size_t fixed = extra(T, 0);
   if (fixed + slot > (size_t)dev.max_smem) return FOS_ERR_UNSUPPORTED;
+  auto fits = [&](int n) { return fixed + (size_t)n * slot <= (size_t)dev.max_smem; };
+  auto ctas_at = [&](int n, int *per_sm) {
+    return resident_ctas(dev.index, occ_key, threads, fixed + (size_t)n * slot, occ, per_sm);
+  };
   int stages = 1;
   if (bulk) {
     if (l && l->stages) {
       stages = l->stages;
-    } else {
-      stages = (int)(stage_target / slot);
-      stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+      if (!fits(stages)) return FOS_ERR_UNSUPPORTED;
+    } else if (fits(2)) {
+      // The rows being computed, not the rows being copied, bound these kernels: take the
+      // deepest ring (up to stage_target bytes, 8 rows) that keeps as many CTAs resident
+      // per SM as a two-row ring does.
+      int cap = (int)(stage_target / slot);
+      cap = cap < 2 ? 2 : (cap > 8 ? 8 : cap);
+      while (cap > 2 && !fits(cap)) --cap;
+      int base = 0;
+      if (ctas_at(2, &base) != cudaSuccess) return FOS_ERR_CUDA;
+      stages = 2;
+      for (int n = cap; n > 2; --n) {
+        int c = 0;
+        if (ctas_at(n, &c) != cudaSuccess) return FOS_ERR_CUDA;
+        if (c >= base) {
+          stages = n;
+          break;
+        }
+      }
     }
-    while (stages > 1 && fixed + stages * slot > (size_t)dev.max_smem) --stages;
-    if (l && l->stages && stages != l->stages) return FOS_ERR_UNSUPPORTED;
   }
   const size_t smem = fixed + stages * slot;
 
@@ -145,7 +194,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
     grid = l->ctas;
   } else {
     int per_sm = 0;
-    if (occ((warps + 1) * 32, smem, &per_sm) != cudaSuccess) return FOS_ERR_CUDA;
+    if (ctas_at(stages, &per_sm) != cudaSuccess) return FOS_ERR_CUDA;
     if (per_sm < 1) return FOS_ERR_UNSUPPORTED;
     grid = per_sm * dev.sms;
   }
@@ -170,7 +219,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   ra->need_geo = (d->causal || d->kv_valid_len || d->key_mask) ? 1 : 0;
   ra->err = dev.err;
 
-  pl->threads = (warps + 1) * 32;  // the compute warps and one producer warp
+  pl->threads = threads;
   pl->grid = grid;
   pl->smem = smem;
   pl->stages = stages;
@@ -210,9 +259,10 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask && !desc->sink &&
                     aligned16(scores) && aligned16(probs) && ((desc->ld * esz) & 15) == 0 &&
                     (((int64_t)desc->key_len * esz) & 15) == 0;
-  // ring of about 24 KB per CTA: rows are consumed right after their tile pass
+  // ring of up to 24 KB per CTA: rows are consumed right after their tile pass
+  const uint32_t key = 0x100u | ((uint32_t)dtype << 4) | ((uint32_t)kt << 1) | (fast ? 1u : 0u);
   st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem, warps, 24 * 1024,
-                 [dtype, kt, fast](int th, size_t sm, int *n) {
+                 key, [dtype, kt, fast](int th, size_t sm, int *n) {
                    return fwd_occupancy(dtype, kt, fast, th, sm, n);
                  },
                  &a, &pl);
@@ -250,6 +300,7 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
                     ((desc->ld * esz) & 15) == 0 && (((int64_t)desc->key_len * esz) & 15) == 0;
   st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
                  bwd_default_warps((desc->key_len + kTileK - 1) / kTileK), 48 * 1024,
+                 0x200u | ((uint32_t)dtype << 4) | (fast ? 1u : 0u),
                  [dtype, fast](int th, size_t sm, int *n) {
                    return bwd_occupancy(dtype, fast, th, sm, n);
                  },

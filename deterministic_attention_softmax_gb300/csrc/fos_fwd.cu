@@ -325,20 +325,24 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
         // flushing these factors cannot change S (see scale_ftz)
         const float alpha = scale_ftz(prev, pm);
         const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
+        // The fold itself is sequential: every lane reads the factors back from shared
+        // memory (broadcast 16-byte reads) and runs the same chain.  Slots past the last
+        // tile hold (1, 0), an exact no-op on S (S * 1 = S, S + 0 = S), so the chain always
+        // runs in steps of four.  tc doubles as the scratch: it is rewritten after the fold.
         const int n = min(32, Te - base);
+        float *ab = tc;
+        ab[lane] = (lane < n) ? alpha : 1.0f;
+        ab[32 + lane] = (lane < n) ? beta : 0.0f;
+        __syncwarp();
         for (int q0 = 0; q0 < n; q0 += 4) {
-          float av[4], bv[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            av[i] = __shfl_sync(kFull, alpha, q0 + i);
-            bv[i] = __shfl_sync(kFull, beta, q0 + i);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float ns = __fadd_rn(__fmul_rn(S, av[i]), bv[i]);
-            S = (q0 + i < n) ? ns : S;
-          }
+          const float4 av = *reinterpret_cast<const float4 *>(ab + q0);
+          const float4 bv = *reinterpret_cast<const float4 *>(ab + 32 + q0);
+          S = __fadd_rn(__fmul_rn(S, av.x), bv.x);
+          S = __fadd_rn(__fmul_rn(S, av.y), bv.y);
+          S = __fadd_rn(__fmul_rn(S, av.z), bv.z);
+          S = __fadd_rn(__fmul_rn(S, av.w), bv.w);
         }
+        __syncwarp();
         M = __shfl_sync(kFull, pm, n - 1);
       }
       for (int t = lane; t < Te; t += 32) {
@@ -414,7 +418,9 @@ const void *fwd_fn(fos_dtype dt, int kt, bool fast) {
 
 size_t fwd_extra_smem(int T, int stages) {
   (void)stages;
-  return (size_t)kBarBytes + kGeoBytes + (size_t)3 * ((T + 3) & ~3) * sizeof(float);
+  // tm and ts (T rounded up to 4), then tc, which is also the merge's 64-float scratch
+  const int T4 = (T + 3) & ~3;
+  return (size_t)kBarBytes + kGeoBytes + (size_t)(2 * T4 + (T4 > 64 ? T4 : 64)) * sizeof(float);
 }
 
 int fwd_tiles_per_warp(int T, int warps) {
@@ -427,8 +433,18 @@ int fwd_tiles_per_warp(int T, int warps) {
 }
 
 int fwd_default_warps(int T) {
-  const int w = (T + 5) / 6;  // up to six tiles (three pairs) per warp
-  return w < 1 ? 1 : (w > 16 ? 16 : w);
+  // Fitted to timings of the unmasked and causal bf16 forward on GB300 over 256..16384 keys
+  // (any choice gives the same bits).  The CTA count per SM is set by the registers that hold
+  // e_j, so the aim is few idle tile slots with two to six tiles per warp.
+  if (T <= 1) return 1;
+  if (T <= 4) return 2;
+  if (T <= 6) return 3;
+  if (T <= 8) return 2;
+  if (T <= 16) return (T + 3) / 4;  // four tiles per warp
+  if (T <= 24) return (T + 5) / 6;  // six
+  if (T <= 32) return (T + 3) / 4;  // four
+  if (T <= 48) return 8;            // six
+  return 6;                         // e_j recomputed in the second pass
 }
 
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
