@@ -425,25 +425,21 @@ def run_ours(args):
     # ---- end to end through the public Python API with pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
+        # the host-buffer entry point: chunked uploads, kernels and downloads overlapped
         hx = sets[0]["x"].cpu().pin_memory()
         hdp = sets[0]["dp"].cpu().pin_memory()
         hp = torch.empty_like(hx).pin_memory()
         hds = torch.empty_like(hx).pin_memory()
         hl = torch.empty(w.rows, dtype=torch.float32).pin_memory()
         hd = torch.empty(w.rows, dtype=torch.float32).pin_memory()
-        dx, ddp = torch.empty_like(sets[0]["x"]), torch.empty_like(sets[0]["dp"])
+        hsk = None if sink is None else torch.empty(w.heads, dtype=torch.float32).pin_memory()
+        ws = torch.empty(fos.fos_step_host_workspace_bytes(hx, batch=w.batch, heads=w.heads,
+                                                           q_len=w.q_len),
+                         dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            dx.copy_(hx, non_blocking=True)
-            ddp.copy_(hdp, non_blocking=True)
-            p, lse = fos.fos_softmax_fwd(dx, sink=sink, **geo)
-            ds, delta = fos.fos_softmax_bwd(p, ddp, **geo)
-            if sink is not None:
-                fos.fos_sink_grad(lse, delta, sink, batch=w.batch, heads=w.heads, q_len=w.q_len)
-            hp.copy_(p, non_blocking=True)
-            hds.copy_(ds, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-            hd.copy_(delta, non_blocking=True)
+            fos.fos_softmax_step_host(hx, hdp, hp, hl, hds, hd, sink=sink, d_sink=hsk,
+                                      workspace=ws, **geo)
 
         for _ in range(3):
             e2e_step()
@@ -459,7 +455,7 @@ def run_ours(args):
         e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.e2e_steps, dev)
         h2d = hx.numel() * hx.element_size() + hdp.numel() * hdp.element_size()
         d2h = (hp.numel() * hp.element_size() + hds.numel() * hds.element_size() +
-               hl.numel() * 4 + hd.numel() * 4)
+               hl.numel() * 4 + hd.numel() * 4 + (0 if hsk is None else hsk.numel() * 4))
         e2e = {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": args.e2e_steps}

@@ -9,9 +9,11 @@ sink gradient without atomics.  The compute lives in ``libfos_softmax.so`` (C AB
 
 from ._build import build
 from .binding import (FosError, Launch, fos_contract_fingerprint, fos_device_error,
-                      fos_sink_grad, fos_softmax_bwd, fos_softmax_fwd, fos_status_string)
+                      fos_sink_grad, fos_softmax_bwd, fos_softmax_fwd, fos_softmax_step_host,
+                      fos_status_string, fos_step_host_workspace_bytes)
 
 __all__ = [
     "FosError", "Launch", "build", "fos_contract_fingerprint", "fos_device_error",
-    "fos_sink_grad", "fos_softmax_bwd", "fos_softmax_fwd", "fos_status_string",
+    "fos_sink_grad", "fos_softmax_bwd", "fos_softmax_fwd", "fos_softmax_step_host",
+    "fos_status_string", "fos_step_host_workspace_bytes",
 ]

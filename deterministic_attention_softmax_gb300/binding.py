@@ -218,6 +218,87 @@ def fos_sink_grad(lse, delta, sink, d_sink=None, *, batch, heads, q_len, key_len
     return d_sink
 
 
+def _check_host(t, name):
+    if t is not None and t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+
+
+def fos_step_host_workspace_bytes(scores, *, batch=None, heads=None, q_len=None,
+                                  chunk_rows: int = 0) -> int:
+    """Device workspace bytes ``fos_softmax_step_host`` needs for the problem of ``scores``
+    (host arithmetic only; 0 for an empty problem)."""
+    if scores.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {scores.dtype}")
+    rows, L, ld, batch, heads, q_len = _geometry(scores, batch, heads, q_len)
+    d = _abi.FosDesc(rows, ld, L, batch, heads, q_len, 0, 0, None, None, None)
+    return int(_abi.lib().fos_step_host_workspace_bytes(ctypes.byref(d), _DTYPES[scores.dtype],
+                                                        int(chunk_rows)))
+
+
+def fos_softmax_step_host(scores, dprobs, probs=None, lse=None, dscores=None, delta=None, *,
+                          batch=None, heads=None, q_len=None, causal=False, kv_valid_len=None,
+                          key_mask=None, sink=None, d_sink=None, want_d_sink=True,
+                          workspace=None, chunk_rows: int = 0, device=None, stream=None,
+                          launch: Launch | None = None):
+    """Forward, backward and (with a sink) sink gradient of host-resident data, through the
+    library's chunked upload / compute / download pipeline.  ``scores``, ``dprobs`` and the
+    outputs are CPU tensors (page-locked ones let the copies overlap; new outputs are
+    allocated page-locked); ``kv_valid_len``, ``key_mask``, ``sink`` and ``workspace`` are
+    CUDA tensors of the device that runs the step.  Returns ``(probs, lse, dscores, delta,
+    d_sink)`` (``d_sink`` is None without a sink); they are complete once the stream is."""
+    if scores.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {scores.dtype}")
+    if device is None:
+        for t in (workspace, sink, kv_valid_len, key_mask):
+            if t is not None and t.is_cuda:
+                device = t.device
+                break
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    rows, L, ld, batch, heads, q_len = _geometry(scores, batch, heads, q_len)
+    _same_layout(scores, dprobs, "scores", "dprobs")
+
+    def host_like(t):
+        return torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, pin_memory=True)
+
+    probs = host_like(scores) if probs is None else probs
+    dscores = host_like(scores) if dscores is None else dscores
+    _same_layout(scores, probs, "scores", "probs")
+    _same_layout(scores, dscores, "scores", "dscores")
+    if lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, pin_memory=True)
+    if delta is None:
+        delta = torch.empty(rows, dtype=torch.float32, pin_memory=True)
+    for t, n in ((lse, "lse"), (delta, "delta")):
+        if t.dtype != torch.float32 or t.numel() != rows or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 tensor with one entry per row")
+    if sink is not None and want_d_sink and d_sink is None:
+        d_sink = torch.empty(heads, dtype=torch.float32, pin_memory=True)
+    if d_sink is not None and (d_sink.dtype != torch.float32 or d_sink.numel() != heads or
+                               not d_sink.is_contiguous()):
+        raise ValueError("d_sink must be a contiguous float32 tensor [heads]")
+    for t, n in ((scores, "scores"), (dprobs, "dprobs"), (probs, "probs"), (dscores, "dscores"),
+                 (lse, "lse"), (delta, "delta"), (d_sink, "d_sink")):
+        _check_host(t, n)
+    for t, n in ((kv_valid_len, "kv_valid_len"), (key_mask, "key_mask"), (sink, "sink"),
+                 (workspace, "workspace")):
+        _check_cuda(t, n, dev)
+    d = _desc(rows, L, ld, batch, heads, q_len, causal, kv_valid_len, key_mask, sink)
+    dt = _DTYPES[scores.dtype]
+    need = int(_abi.lib().fos_step_host_workspace_bytes(ctypes.byref(d), dt, int(chunk_rows)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_softmax_step_host(
+            ctypes.byref(d), dt, _ptr(scores), _ptr(dprobs), _ptr(probs), _ptr(lse),
+            _ptr(dscores), _ptr(delta), _ptr(d_sink), _ptr(workspace), ws_bytes,
+            int(chunk_rows), _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_softmax_step_host")
+    return probs, lse, dscores, delta, d_sink
+
+
 def fos_device_error(stream=None, device=None) -> int:
     """Synchronise the stream and return (and clear) the device error status code."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device

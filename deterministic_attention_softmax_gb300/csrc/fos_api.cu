@@ -20,7 +20,6 @@ __device__ unsigned g_device_error;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kBarBytes = 128;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultWarps = 8;
 
@@ -63,6 +62,8 @@ fos_status device_info(DevInfo **out) {
   return FOS_OK;
 }
 
+}  // namespace
+
 int dtype_size(fos_dtype dt) {
   switch (dt) {
     case FOS_F32: return 4;
@@ -71,8 +72,6 @@ int dtype_size(fos_dtype dt) {
   }
   return 0;
 }
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 fos_status check_desc(const fos_desc *d) {
   if (d == nullptr) return FOS_ERR_INVALID;
@@ -99,6 +98,10 @@ fos_status check_launch(const fos_launch *l) {
   if (l->generic != 0 && l->generic != 1) return FOS_ERR_INVALID;
   return FOS_OK;
 }
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Resident CTAs per SM of a kernel instance at a block size and dynamic shared memory,
 // memoised: a launch asks for up to eight ring depths and the answer never changes.
@@ -138,7 +141,8 @@ struct Plan {
 // Fills the shared part of RowArgs and picks path, stages, CTAs.  `inputs` are the row
 // arrays that are staged (scores, or P and dP); `copies` is how many of them a stage holds.
 template <typename OccFn>
-fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs, int copies,
+fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
+                     const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
                      size_t (*extra)(int, int), int default_warps, size_t stage_target,
                      uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl) {
@@ -198,9 +202,10 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
     if (per_sm < 1) return FOS_ERR_UNSUPPORTED;
     grid = per_sm * dev.sms;
   }
-  if ((int64_t)grid > d->rows) grid = (int)d->rows;
+  if ((int64_t)grid > nrows) grid = (int)nrows;
 
-  ra->rows = d->rows;
+  ra->rows = nrows;
+  ra->row_base = row_base;
   ra->ld = d->ld;
   ra->L = d->key_len;
   ra->heads = d->heads;
@@ -217,6 +222,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
   ra->timeout_ns = (l && l->wait_timeout_ns) ? (uint64_t)l->wait_timeout_ns : kDefaultTimeoutNs;
   ra->test_stall = l ? l->test_stall : 0;
   ra->need_geo = (d->causal || d->kv_valid_len || d->key_mask) ? 1 : 0;
+  ra->geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
   ra->err = dev.err;
 
   pl->threads = threads;
@@ -232,17 +238,14 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, const void *const *inputs,
 
 using namespace fos;
 
-extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
-                                      void *probs, float *lse, cudaStream_t stream,
-                                      const fos_launch *launch) {
-  fos_status st = check_desc(desc);
-  if (st != FOS_OK) return st;
-  if ((st = check_launch(launch)) != FOS_OK) return st;
-  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
-  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
-  if (scores == nullptr || probs == nullptr || lse == nullptr) return FOS_ERR_INVALID;
+namespace fos {
+
+fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
+                   const void *scores, void *probs, float *lse, cudaStream_t stream,
+                   const fos_launch *launch) {
   DevInfo *dev = nullptr;
-  if ((st = device_info(&dev)) != FOS_OK) return st;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
 
   FwdArgs a{};
   Plan pl;
@@ -261,8 +264,8 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
                     (((int64_t)desc->key_len * esz) & 15) == 0;
   // ring of up to 24 KB per CTA: rows are consumed right after their tile pass
   const uint32_t key = 0x100u | ((uint32_t)dtype << 4) | ((uint32_t)kt << 1) | (fast ? 1u : 0u);
-  st = plan_rows(desc, dtype, inputs, 1, probs, launch, *dev, fwd_extra_smem, warps, 24 * 1024,
-                 key, [dtype, kt, fast](int th, size_t sm, int *n) {
+  st = plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev, fwd_extra_smem,
+                 warps, 24 * 1024, key, [dtype, kt, fast](int th, size_t sm, int *n) {
                    return fwd_occupancy(dtype, kt, fast, th, sm, n);
                  },
                  &a, &pl);
@@ -278,17 +281,12 @@ extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, con
   return FOS_OK;
 }
 
-extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *probs,
-                                      const void *dprobs, void *dscores, float *delta,
-                                      cudaStream_t stream, const fos_launch *launch) {
-  fos_status st = check_desc(desc);
-  if (st != FOS_OK) return st;
-  if ((st = check_launch(launch)) != FOS_OK) return st;
-  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
-  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
-  if (probs == nullptr || dprobs == nullptr || dscores == nullptr) return FOS_ERR_INVALID;
+fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
+                   const void *probs, const void *dprobs, void *dscores, float *delta,
+                   cudaStream_t stream, const fos_launch *launch) {
   DevInfo *dev = nullptr;
-  if ((st = device_info(&dev)) != FOS_OK) return st;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
 
   BwdArgs a{};
   Plan pl;
@@ -298,7 +296,7 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask &&
                     aligned16(probs) && aligned16(dprobs) && aligned16(dscores) &&
                     ((desc->ld * esz) & 15) == 0 && (((int64_t)desc->key_len * esz) & 15) == 0;
-  st = plan_rows(desc, dtype, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
+  st = plan_rows(desc, dtype, row_base, nrows, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
                  bwd_default_warps((desc->key_len + kTileK - 1) / kTileK), 48 * 1024,
                  0x200u | ((uint32_t)dtype << 4) | (fast ? 1u : 0u),
                  [dtype, fast](int th, size_t sm, int *n) {
@@ -316,18 +314,11 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
   return FOS_OK;
 }
 
-extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
-                                    float *d_sink, cudaStream_t stream,
-                                    const fos_launch *launch) {
-  fos_status st = check_desc(desc);
-  if (st != FOS_OK) return st;
-  if ((st = check_launch(launch)) != FOS_OK) return st;
-  if (desc->sink == nullptr || lse == nullptr || delta == nullptr || d_sink == nullptr)
-    return FOS_ERR_INVALID;
-  if (desc->heads == 0) return FOS_OK;
-  if (desc->rows == 0) return FOS_ERR_INVALID;  // heads > 0 with no rows: nothing defines d_sink
+fos_status run_sink(const fos_desc *desc, const float *lse, const float *delta, float *d_sink,
+                    cudaStream_t stream, const fos_launch *launch) {
   DevInfo *dev = nullptr;
-  if ((st = device_info(&dev)) != FOS_OK) return st;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
   SinkArgs a{};
   a.batch = desc->batch;
   a.heads = desc->heads;
@@ -339,6 +330,45 @@ extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, cons
   const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
   if (sink_launch(a, warps * 32, stream) != cudaSuccess) return FOS_ERR_CUDA;
   return FOS_OK;
+}
+
+}  // namespace fos
+
+extern "C" fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
+                                      void *probs, float *lse, cudaStream_t stream,
+                                      const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
+  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
+  if (scores == nullptr || probs == nullptr || lse == nullptr) return FOS_ERR_INVALID;
+  return run_fwd(desc, dtype, 0, desc->rows, scores, probs, lse, stream, launch);
+}
+
+extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *probs,
+                                      const void *dprobs, void *dscores, float *delta,
+                                      cudaStream_t stream, const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
+  if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
+  if (probs == nullptr || dprobs == nullptr || dscores == nullptr) return FOS_ERR_INVALID;
+  return run_bwd(desc, dtype, 0, desc->rows, probs, dprobs, dscores, delta, stream, launch);
+}
+
+extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
+                                    float *d_sink, cudaStream_t stream,
+                                    const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (desc->sink == nullptr || lse == nullptr || delta == nullptr || d_sink == nullptr)
+    return FOS_ERR_INVALID;
+  if (desc->heads == 0) return FOS_OK;
+  if (desc->rows == 0) return FOS_ERR_INVALID;  // heads > 0 with no rows: nothing defines d_sink
+  return run_sink(desc, lse, delta, d_sink, stream, launch);
 }
 
 extern "C" fos_status fos_device_error(cudaStream_t stream) {

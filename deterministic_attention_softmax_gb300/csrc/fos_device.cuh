@@ -216,15 +216,17 @@ __device__ __forceinline__ void store_lane8(unsigned char *row, int j0, int L, b
 
 // ------------------------------------------------------------------ row geometry and masks
 
-// Rows are ordered [batch][heads][q_len].  Returns {lim, b, h, 0}: lim is the number of
-// leading keys of row r that can be valid (causal bound and valid length; key_mask and -inf
+// Rows are ordered [batch][heads][q_len]; local row r of a launch is problem row
+// a.row_base + r.  Returns {lim, b, h, 0}: lim is the number of leading keys of the row that
+// can be valid (causal bound and valid length; key_mask and -inf
 // are applied per key), b and h its batch entry and head.  Only computed when a mask or a
 // sink needs it (one thread per row calls this, when it issues the row's copy).
 __device__ __forceinline__ int4 row_geometry(const RowArgs &a, int64_t r) {
   int4 g = make_int4(a.L, 0, 0, 0);
   if (!a.need_geo) return g;
+  r += a.row_base;
   int64_t b, h, i;
-  if (a.rows <= 0x7fffffffLL) {  // 32-bit arithmetic suffices
+  if (a.geo32) {  // 32-bit arithmetic suffices
     const uint32_t rr = (uint32_t)r, q = rr / (uint32_t)a.q_len;
     i = rr - q * (uint32_t)a.q_len;
     b = q / (uint32_t)a.heads;

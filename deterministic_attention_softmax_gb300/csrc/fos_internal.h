@@ -14,7 +14,8 @@ constexpr int kTileK = 256;  // keys per tile: part of the arithmetic contract
 
 // Geometry and masks shared by the forward and backward row kernels.
 struct RowArgs {
-  int64_t rows;
+  int64_t rows;                // rows of this launch
+  int64_t row_base;            // problem row of local row 0 (a launch may cover a row range)
   int64_t ld;                  // elements between row starts
   int32_t L;                   // key length
   int32_t heads, q_len, causal;
@@ -29,6 +30,7 @@ struct RowArgs {
   uint64_t timeout_ns;         // limit of every bounded wait
   int32_t test_stall;          // test only: CTA 0 never issues its first copy
   int32_t need_geo;            // rows need b / h / limit (a mask or a sink is given)
+  int32_t geo32;               // row_base + rows fits in int32: 32-bit geometry arithmetic
   unsigned *err;               // device error word
 };
 
@@ -77,5 +79,22 @@ cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int 
                        size_t smem, cudaStream_t s);
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
+
+// Host-side checks shared by the C ABI entry points (fos_api.cu).
+int dtype_size(fos_dtype dt);
+fos_status check_desc(const fos_desc *d);
+fos_status check_launch(const fos_launch *l);
+
+// The three operations on already validated arguments.  run_fwd / run_bwd cover rows
+// [row_base, row_base + nrows) of the problem in d; their array pointers address local row 0
+// of that range (lse / delta included), while masks and sink keep their problem-wide indexing.
+fos_status run_fwd(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
+                   const void *scores, void *probs, float *lse, cudaStream_t s,
+                   const fos_launch *l);
+fos_status run_bwd(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
+                   const void *probs, const void *dprobs, void *dscores, float *delta,
+                   cudaStream_t s, const fos_launch *l);
+fos_status run_sink(const fos_desc *d, const float *lse, const float *delta, float *d_sink,
+                    cudaStream_t s, const fos_launch *l);
 
 }  // namespace fos

@@ -38,10 +38,13 @@
  * fos_contract_fingerprint() spells out the full contract as a string.
  *
  * Ownership and streams.  The caller owns every buffer; all array pointers are DEVICE
- * pointers.  The library allocates no memory, keeps no per-call state and never synchronises
- * (fos_device_error excepted): each call validates its arguments on the host, enqueues its
- * kernel on `stream` on the current device and returns.  Output buffers must not overlap
- * inputs, except that probs may equal scores and dscores may equal dprobs (in place).
+ * pointers, except the data arrays of fos_softmax_step_host, which are HOST pointers.  The
+ * library allocates no memory and never synchronises (fos_device_error excepted): each call
+ * validates its arguments on the host, enqueues its work on `stream` on the current device
+ * and returns.  The only state kept across calls is per device: kernel attributes, the
+ * device error word, and the two streams and events of the host-buffer pipeline.  Output
+ * buffers must not overlap inputs, except that probs may equal scores and dscores may equal
+ * dprobs (in place).
  *
  * Errors.  Every entry point returns fos_status:
  *   FOS_ERR_INVALID      bad arguments (null required pointer, rows != batch*heads*q_len,
@@ -57,6 +60,7 @@
 #ifndef FOS_SOFTMAX_H
 #define FOS_SOFTMAX_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #include <cuda_runtime_api.h> /* cudaStream_t */
@@ -100,7 +104,7 @@ typedef struct fos_desc {
  * they exist so that tests can vary the launch geometry and exercise the bounded-wait path.
  */
 typedef struct fos_launch {
-  int32_t warps_per_cta; /* 0 = default (8); otherwise 1..16 */
+  int32_t warps_per_cta; /* 0 = default (chosen from key_len); otherwise 1..16 */
   int32_t ctas;          /* 0 = default (persistent: SMs x resident CTAs); else >= 1 */
   int32_t stages;        /* 0 = default; rows in flight per CTA on the bulk-copy path, 1..16 */
   int32_t load_path;     /* 0 = auto, 1 = bulk copy (TMA) only, 2 = plain loads only */
@@ -152,6 +156,46 @@ fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *pr
  */
 fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
                          float *d_sink, cudaStream_t stream, const fos_launch *launch);
+
+/*
+ * The forward, the backward and (when d_sink is given) the sink gradient of one batch whose
+ * data live in HOST memory: the same results, bit for bit, as fos_softmax_fwd on a device
+ * copy of scores, fos_softmax_bwd on the P it produced and dprobs, and fos_sink_grad, with
+ * every outcome copied back.  Rows are processed in chunks of `chunk_rows` (0 = about 16 MB
+ * of one tensor per chunk) that cycle through three slots of `workspace`: the upload of one
+ * chunk, the kernels of the previous one and the download of the one before that overlap on
+ * three streams (two of them the library's own, ordered against `stream` by events).  This is
+ * the data movement a caller with host-resident data needs around the softmax ("Batch-
+ * invariant attention (standard softmax--cuda version)", Acceptance Criteria: the outputs
+ * must not depend on how rows are batched; here they do not depend on the chunking either).
+ *   scores, dprobs        host [rows, ld] of dtype  (inputs; page-locked memory lets the
+ *                         copies overlap, pageable memory is correct but serialises them)
+ *   probs, dscores        host [rows, ld] of dtype  (outputs; columns key_len..ld-1 of the
+ *                         host rows are not written)
+ *   lse, delta            host float [rows]         (outputs)
+ *   d_sink                host float [heads] or NULL (output; needs desc->sink)
+ *   desc->kv_valid_len, key_mask, sink stay DEVICE pointers, as in the other calls.
+ *   workspace             device, 256-byte aligned, at least
+ *                         fos_step_host_workspace_bytes(desc, dtype, chunk_rows) bytes;
+ *                         owned by the caller, not to be touched until `stream` completes.
+ * The call returns once everything is enqueued; the outputs are complete when `stream` is.
+ * FOS_ERR_INVALID also for a missing or too small or misaligned workspace, a negative
+ * chunk_rows, or d_sink without a sink.  rows == 0 is valid and enqueues nothing.  On
+ * FOS_ERR_CUDA part of the pipeline may already be enqueued; the outputs are then undefined.
+ */
+fos_status fos_softmax_step_host(const fos_desc *desc, fos_dtype dtype, const void *scores,
+                                 const void *dprobs, void *probs, float *lse, void *dscores,
+                                 float *delta, float *d_sink, void *workspace,
+                                 size_t workspace_bytes, int64_t chunk_rows, cudaStream_t stream,
+                                 const fos_launch *launch);
+
+/*
+ * Device workspace bytes fos_softmax_step_host needs for this problem and chunk size
+ * (0 = the default chunk): the full LSE and delta arrays, d_sink, and three slots of two
+ * chunk tensors.  Host arithmetic only (no CUDA call).  Returns 0 for an invalid
+ * description, dtype or chunk_rows, and for rows == 0.
+ */
+size_t fos_step_host_workspace_bytes(const fos_desc *desc, fos_dtype dtype, int64_t chunk_rows);
 
 /*
  * Synchronises `stream`, then reports and clears the device error word of the current

@@ -125,3 +125,41 @@ def test_binding_refuses_cpu_tensors():
     fos.build()
     with pytest.raises(ValueError):
         fos.fos_softmax_fwd(torch.zeros(4, 8))
+
+
+def test_step_host_workspace_bytes(abi):
+    lib = abi.lib()
+    d = _desc(abi)  # 6 rows x 8 keys, 2 heads
+    # LSE, delta and d_sink (256-byte aligned each), then 3 slots x 2 chunk tensors
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(d), abi.FOS_BF16, 0) == 3 * 256 + 6 * 256
+    big = _desc(abi, rows=4096, batch=1, heads=1, q_len=4096, ld=1000, key_len=1000)
+    chunk = 100  # 100 rows of 2000 bytes -> 200,192 bytes per tensor after alignment
+    t = -(-100 * 1000 * 2 // 256) * 256
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(big), abi.FOS_BF16, chunk) == \
+        2 * 16384 + 256 + 6 * t
+    # the default chunk is about 16 MB of one tensor, capped at the row count
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(big), abi.FOS_F32, 0) == \
+        2 * 16384 + 256 + 6 * (4096 * 4000)
+    for bad in (dict(rows=7), dict(ld=7)):
+        assert lib.fos_step_host_workspace_bytes(ctypes.byref(_desc(abi, **bad)), abi.FOS_BF16, 0) == 0
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(d), 9, 0) == 0
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(d), abi.FOS_BF16, -1) == 0
+    assert lib.fos_step_host_workspace_bytes(ctypes.byref(_desc(abi, rows=0, batch=0)),
+                                             abi.FOS_BF16, 0) == 0
+
+
+def test_step_host_refuses_before_any_cuda_call(abi):
+    lib = abi.lib()
+    d = _desc(abi)
+    need = lib.fos_step_host_workspace_bytes(ctypes.byref(d), abi.FOS_BF16, 0)
+    ws = ctypes.c_void_p(0x10000)  # 256-byte aligned, never dereferenced
+    call = lambda dd, ws_, n, chunk=0, dsink=None: lib.fos_softmax_step_host(
+        ctypes.byref(dd), abi.FOS_BF16, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dsink, ws_, n, chunk,
+        None, None)
+    assert call(d, ws, need - 1) == abi.FOS_ERR_INVALID          # workspace too small
+    assert call(d, ctypes.c_void_p(0x10010), need) == abi.FOS_ERR_INVALID  # misaligned
+    assert call(d, None, need) == abi.FOS_ERR_INVALID            # no workspace
+    assert call(d, ws, need, chunk=-3) == abi.FOS_ERR_INVALID
+    assert call(d, ws, need, dsink=FAKE) == abi.FOS_ERR_INVALID  # d_sink without a sink
+    assert call(_desc(abi, rows=7), ws, need) == abi.FOS_ERR_INVALID
+    assert call(_desc(abi, rows=0, batch=0), None, 0) == abi.FOS_OK  # empty: nothing enqueued
