@@ -22,8 +22,8 @@ STATUS_NAMES = {0: "FOS_OK", 1: "FOS_ERR_INVALID", 2: "FOS_ERR_UNSUPPORTED", 3: 
 
 # Every symbol include/fos_softmax.h declares.
 EXPORTED = ("fos_softmax_fwd", "fos_softmax_bwd", "fos_sink_grad", "fos_softmax_step_host",
-            "fos_step_host_workspace_bytes", "fos_device_error", "fos_status_string",
-            "fos_contract_fingerprint")
+            "fos_step_host_workspace_bytes", "fos_softmax_step_host_static", "fos_device_error",
+            "fos_status_string", "fos_contract_fingerprint")
 
 
 class FosDesc(ctypes.Structure):
@@ -83,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.fos_softmax_step_host.restype = ctypes.c_int
         L.fos_step_host_workspace_bytes.argtypes = [dp, ctypes.c_int, ctypes.c_int64]
         L.fos_step_host_workspace_bytes.restype = ctypes.c_size_t
+        L.fos_softmax_step_host_static.argtypes = [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                                   ctypes.c_int64, vp, lp]
+        L.fos_softmax_step_host_static.restype = ctypes.c_int
         L.fos_device_error.argtypes = [vp]
         L.fos_device_error.restype = ctypes.c_int
         L.fos_status_string.argtypes = [ctypes.c_int]

@@ -194,3 +194,80 @@ extern "C" fos_status fos_softmax_step_host(const fos_desc *desc, fos_dtype dtyp
 #undef FOS_CU
   return FOS_OK;
 }
+
+// ----------------------------------------------------------------- the allocation-free variant
+//
+// Some callers cannot allocate device memory for the step's workspace: a host application
+// whose memory manager has already reserved the device memory it is allowed (a serving
+// engine that pre-allocates its cache pool, a framework whose caching allocator must see every
+// block), or a code path where cudaMalloc / cudaFree are not acceptable because cudaFree
+// synchronises the device.  fos_softmax_step_host_static serves them with a fixed scratch
+// array that is part of the library image: every GPU that loads the library holds it until the
+// process exits.  Calls share it, so calls that overlap on the GPU (two streams with no order
+// between them) race; calls on one stream are ordered.  Nothing in it needs to start at zero:
+// every byte a call reads there was written earlier in the same call.
+
+namespace fos {
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;  // FOS_STEP_HOST_STATIC_SCRATCH_BYTES
+static_assert(kStaticScratchBytes == FOS_STEP_HOST_STATIC_SCRATCH_BYTES, "header and library disagree");
+
+static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
+
+// Device address of g_step_scratch per device, taken once with that device current (in host
+// code the array's name is only a host-side stand-in).
+void *g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+fos_status static_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FOS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FOS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_step_scratch) != cudaSuccess || p == nullptr)
+      return FOS_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return FOS_OK;
+}
+
+}  // namespace
+}  // namespace fos
+
+extern "C" fos_status fos_softmax_step_host_static(const fos_desc *desc, fos_dtype dtype,
+                                                   const void *scores, const void *dprobs,
+                                                   void *probs, float *lse, void *dscores,
+                                                   float *delta, float *d_sink,
+                                                   int64_t chunk_rows, cudaStream_t stream,
+                                                   const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  const int esz = dtype_size(dtype);
+  if (esz == 0 || chunk_rows < 0) return FOS_ERR_INVALID;
+  if (desc->rows == 0) {
+    return fos_softmax_step_host(desc, dtype, scores, dprobs, probs, lse, dscores, delta, d_sink,
+                                 nullptr, 0, chunk_rows, stream, launch);
+  }
+  int64_t chunk = chunk_rows;
+  if (chunk == 0) {
+    // the default chunk, shrunk until the whole workspace fits the static array (the
+    // 256-byte rounding of the slots costs at most a few more rows)
+    const size_t fixed = layout(desc, esz, 1).slot0;
+    if (fixed >= kStaticScratchBytes) return FOS_ERR_UNSUPPORTED;
+    const size_t row_bytes = (size_t)desc->ld * esz;
+    const int64_t fit = (int64_t)((kStaticScratchBytes - fixed) / (2 * kSlots) / row_bytes);
+    chunk = layout(desc, esz, 0).chunk;
+    if (fit < chunk) chunk = fit;
+    if (chunk < 1) chunk = 1;
+    while (chunk > 1 && layout(desc, esz, chunk).total > kStaticScratchBytes) --chunk;
+  }
+  if (layout(desc, esz, chunk).total > kStaticScratchBytes) return FOS_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  if ((st = static_scratch(&scratch)) != FOS_OK) return st;
+  return fos_softmax_step_host(desc, dtype, scores, dprobs, probs, lse, dscores, delta, d_sink,
+                               scratch, kStaticScratchBytes, chunk, stream, launch);
+}

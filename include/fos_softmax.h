@@ -197,6 +197,36 @@ fos_status fos_softmax_step_host(const fos_desc *desc, fos_dtype dtype, const vo
  */
 size_t fos_step_host_workspace_bytes(const fos_desc *desc, fos_dtype dtype, int64_t chunk_rows);
 
+/* Bytes of the scratch array built into the library for fos_softmax_step_host_static. */
+#define FOS_STEP_HOST_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fos_softmax_step_host for callers that cannot allocate device memory: no workspace
+ * argument; the step uses a scratch array of FOS_STEP_HOST_STATIC_SCRATCH_BYTES (32 MB) that
+ * is part of the library and held by every GPU that loads it until the process exits.  Made
+ * for a host application whose memory manager already owns the device memory it may use (a
+ * serving engine that reserves its cache pool up front, a framework whose caching allocator
+ * must account for every block), or a code path that must not call cudaMalloc / cudaFree
+ * (cudaFree synchronises the whole device).  It calls neither, nor any routine that allocates
+ * device memory.  The pages describe no counterpart of this entry point: it is data movement
+ * around the softmax, not part of the method.
+ *   Arguments as fos_softmax_step_host, minus the workspace.  chunk_rows = 0 takes the default
+ *   chunk, shrunk until the LSE, delta and d_sink arrays and three slots of two chunk tensors
+ *   fit the array.
+ *   FOS_ERR_UNSUPPORTED when they do not fit even with the given (or a one-row) chunk: roughly
+ *   8 * rows + 4 * heads + 6 * chunk_rows * ld * element size > 32 MB.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ * creates the pipeline's streams and events: make that first call before any stream capture.
+ * Every call uses the same array, so calls that overlap on the GPU (on two streams with no
+ * order between them) race; calls on one stream are ordered.  Nothing in the array needs to
+ * start at zero: each call writes what it reads there.
+ */
+fos_status fos_softmax_step_host_static(const fos_desc *desc, fos_dtype dtype,
+                                        const void *scores, const void *dprobs, void *probs,
+                                        float *lse, void *dscores, float *delta, float *d_sink,
+                                        int64_t chunk_rows, cudaStream_t stream,
+                                        const fos_launch *launch);
+
 /*
  * Synchronises `stream`, then reports and clears the device error word of the current
  * device: FOS_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call, FOS_OK
