@@ -52,13 +52,39 @@ __device__ __forceinline__ float lane_dot(const float (&p)[8], const float (&d)[
   return acc;
 }
 
+// lane_dot of two unmasked tiles at once, packed (.x: first tile, .y: second).  The packed
+// float32 fused multiply-add of the sm_100 family (__ffma2_rn) rounds each component as
+// __fmaf_rn does, so each component has the bits of lane_dot on its own tile.
+__device__ __forceinline__ float2 lane_dot2(const float (&p0)[8], const float (&d0)[8],
+                                            const float (&p1)[8], const float (&d1)[8]) {
+  float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int q = 0; q < kLaneKeys; ++q)
+    acc = __ffma2_rn(make_float2(p0[q], p1[q]), make_float2(d0[q], d1[q]), acc);
+  return acc;
+}
+
+// dScores of the lane's 8 keys: fma(P, dP - delta, +0), +0 for masked keys.  Unmasked tiles
+// take neighbouring keys two at a time in packed form (dP - delta as dP + (-delta), the same
+// IEEE operation; same bits per key).
 __device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[8], int j0,
                                           int lim, const uint8_t *km, bool masked, float delta,
                                           float (&v)[8]) {
+  if (!masked) {
+    const float2 nd = make_float2(-delta, -delta), zero = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < kLaneKeys; q += 2) {
+      const float2 x = __fadd2_rn(make_float2(d[q], d[q + 1]), nd);
+      const float2 g = __ffma2_rn(make_float2(p[q], p[q + 1]), x, zero);
+      v[q] = g.x;
+      v[q + 1] = g.y;
+    }
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < kLaneKeys; ++q) {
     const float g = __fmaf_rn(p[q], __fsub_rn(d[q], delta), 0.0f);
-    v[q] = (!masked || key_ok(j0 + q, lim, km)) ? g : 0.0f;
+    v[q] = key_ok(j0 + q, lim, km) ? g : 0.0f;
   }
 }
 
@@ -135,7 +161,7 @@ __device__ void bwd_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmi
 // kFast: the common case fixed at compile time (bulk copies, no mask, 16-byte aligned output).
 // Both instances do the same arithmetic in the same order.
 template <typename T, bool kFast>
-__global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
+__global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -212,12 +238,18 @@ __global__ void __maxnreg__(64) fos_bwd_kernel(const BwdArgs a) {
         float p0[8], d0[8], p1[8], d1[8];
         tile_pdp<T>(sp, sd, j0, p0, d0);
         tile_pdp<T>(sp, sd, j1, p1, d1);
-        float a0 = lane_dot(p0, d0, j0, lim, km, km != nullptr || (t + 1) * kTileK > lim);
-        float a1 = lane_dot(p1, d1, j1, lim, km, km != nullptr || (t1 + 1) * kTileK > lim);
-        warp_sum_xor2(a0, a1);
+        const bool m0 = km != nullptr || (t + 1) * kTileK > lim;
+        const bool m1 = km != nullptr || (t1 + 1) * kTileK > lim;
+        float2 acc = (m0 || m1) ? make_float2(lane_dot(p0, d0, j0, lim, km, m0),
+                                              lane_dot(p1, d1, j1, lim, km, m1))
+                                : lane_dot2(p0, d0, p1, d1);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)  // the xor tree of both tiles, packed
+          acc = __fadd2_rn(acc, make_float2(__shfl_xor_sync(kFull, acc.x, o),
+                                            __shfl_xor_sync(kFull, acc.y, o)));
         if (lane == 0) {
-          td[t] = a0;
-          td[t1] = a1;
+          td[t] = acc.x;
+          td[t1] = acc.y;
         }
       }
       if (t < Te) {
