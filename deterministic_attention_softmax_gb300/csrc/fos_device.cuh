@@ -50,12 +50,16 @@ __device__ __forceinline__ float scale_fos(float a, float b) {
 // (87 * log2 e < 126), and for the merge's rescale factors, whose subnormal values are always
 // added to a term of at least 1 (the tile or sink holding the running maximum contributes
 // exp(0) = 1), far below half an ulp of it.
-__device__ __forceinline__ float exp_ftz(float d) {
-  const float t = __fmul_rn(d, 1.44269504088896340736f);
+constexpr float kLog2e = 1.44269504088896340736f;  // log2 e rounded to float32
+
+// The base-2 step of exp_ftz alone, for an argument already multiplied by log2 e.
+__device__ __forceinline__ float ex2_ftz(float t) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
   return y;
 }
+
+__device__ __forceinline__ float exp_ftz(float d) { return ex2_ftz(__fmul_rn(d, kLog2e)); }
 
 __device__ __forceinline__ float scale_ftz(float a, float b) {
   return (a == b) ? 1.0f : exp_ftz(__fsub_rn(a, b));

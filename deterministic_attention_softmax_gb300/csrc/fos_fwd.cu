@@ -56,13 +56,22 @@ __device__ __forceinline__ void tile_keys(const unsigned char *stage, int t, int
 // e_j = exp(x_j - m) and their ascending lane sum.  For a tile with no valid key (m = -inf)
 // the shift is -FLT_MAX instead, so every e_j is exp(-inf) = +0; otherwise it is m itself.
 // Unless some key of the tile lies more than 87 below the maximum (a warp-uniform test), no
-// e_j can be below 2^-126 and the flush-to-zero exponential gives the same bits.
+// e_j can be below 2^-126 and the flush-to-zero exponential gives the same bits.  On that
+// path neighbouring keys go two at a time through the packed float32 operations of the
+// sm_100 family (__fadd2_rn, __fmul2_rn), which round each component exactly as the scalar
+// operation does; x - m is computed as x + (-m), the same IEEE operation.
 __device__ __forceinline__ float tile_exp_sum(const float (&x)[8], float m, float (&e)[8]) {
   const float mm = fmaxf(m, -FLT_MAX);
   const bool deep = __any_sync(kFull, __fsub_rn(min8(x), mm) < -87.0f);
   if (!deep) {
+    const float2 neg = make_float2(-mm, -mm);
+    const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
-    for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_ftz(__fsub_rn(x[q], mm));
+    for (int q = 0; q < kLaneKeys; q += 2) {
+      const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[q], x[q + 1]), neg), l2e);
+      e[q] = ex2_ftz(t.x);
+      e[q + 1] = ex2_ftz(t.y);
+    }
   } else {
 #pragma unroll
     for (int q = 0; q < kLaneKeys; ++q) e[q] = exp_fos(__fsub_rn(x[q], mm));
@@ -122,8 +131,13 @@ template <typename T>
 __device__ __forceinline__ void tile_store(unsigned char *prow, int t, int lane, int L, bool ovec,
                                            const float (&e)[8], float c) {
   float v[8];
+  const float2 cc = make_float2(c, c);
 #pragma unroll
-  for (int q = 0; q < kLaneKeys; ++q) v[q] = __fmul_rn(e[q], c);
+  for (int q = 0; q < kLaneKeys; q += 2) {  // packed: one rounding per component
+    const float2 pq = __fmul2_rn(make_float2(e[q], e[q + 1]), cc);
+    v[q] = pq.x;
+    v[q + 1] = pq.y;
+  }
   store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, L, ovec, v);
 }
 
