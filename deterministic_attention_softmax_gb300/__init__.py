@@ -9,11 +9,13 @@ sink gradient without atomics.  The compute lives in ``libfos_softmax.so`` (C AB
 
 from ._build import build
 from .binding import (FosError, Launch, fos_contract_fingerprint, fos_device_error,
-                      fos_sink_grad, fos_softmax_bwd, fos_softmax_fwd, fos_softmax_step_host,
-                      fos_status_string, fos_step_host_workspace_bytes)
+                      fos_sink_grad, fos_sink_grad_merge, fos_sink_grad_partials,
+                      fos_softmax_bwd, fos_softmax_fwd, fos_softmax_step_host,
+                      fos_status_string, fos_step_host_workspace_bytes, sink_chunk_range)
 
 __all__ = [
     "FosError", "Launch", "build", "fos_contract_fingerprint", "fos_device_error",
-    "fos_sink_grad", "fos_softmax_bwd", "fos_softmax_fwd", "fos_softmax_step_host",
-    "fos_status_string", "fos_step_host_workspace_bytes",
+    "fos_sink_grad", "fos_sink_grad_merge", "fos_sink_grad_partials", "fos_softmax_bwd",
+    "fos_softmax_fwd", "fos_softmax_step_host", "fos_status_string",
+    "fos_step_host_workspace_bytes", "sink_chunk_range",
 ]

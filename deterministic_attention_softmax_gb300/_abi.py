@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "FOS_OK", 1: "FOS_ERR_INVALID", 2: "FOS_ERR_UNSUPPORTED", 3: 
                 4: "FOS_ERR_TIMEOUT"}
 
 # Every symbol include/fos_softmax.h declares.
-EXPORTED = ("fos_softmax_fwd", "fos_softmax_bwd", "fos_sink_grad", "fos_softmax_step_host",
+EXPORTED = ("fos_softmax_fwd", "fos_softmax_bwd", "fos_sink_grad", "fos_sink_grad_partials",
+            "fos_sink_grad_merge", "fos_softmax_step_host",
             "fos_step_host_workspace_bytes", "fos_softmax_step_host_static", "fos_device_error",
             "fos_status_string", "fos_contract_fingerprint")
 
@@ -78,6 +79,11 @@ def lib() -> ctypes.CDLL:
         L.fos_softmax_bwd.restype = ctypes.c_int
         L.fos_sink_grad.argtypes = [dp, vp, vp, vp, vp, lp]
         L.fos_sink_grad.restype = ctypes.c_int
+        L.fos_sink_grad_partials.argtypes = [dp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
+                                             lp]
+        L.fos_sink_grad_partials.restype = ctypes.c_int
+        L.fos_sink_grad_merge.argtypes = [ctypes.c_int32, ctypes.c_int64, vp, vp]
+        L.fos_sink_grad_merge.restype = ctypes.c_int
         L.fos_softmax_step_host.argtypes = [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp,
                                             ctypes.c_size_t, ctypes.c_int64, vp, lp]
         L.fos_softmax_step_host.restype = ctypes.c_int

@@ -218,6 +218,57 @@ def fos_sink_grad(lse, delta, sink, d_sink=None, *, batch, heads, q_len, key_len
     return d_sink
 
 
+def sink_chunk_range(q_len: int, batch_begin: int, batch_end: int) -> tuple[int, int]:
+    """[c0, c1): the 256-position chunks of one head covered by batch entries [b0, b1)."""
+    p0, p1 = int(batch_begin) * int(q_len), int(batch_end) * int(q_len)
+    return p0 // 256, -(-p1 // 256)
+
+
+def fos_sink_grad_partials(lse, delta, sink, partials=None, *, batch, heads, q_len,
+                           batch_begin, batch_end, stream=None, launch: Launch | None = None):
+    """Chunk partials ``[heads, c1 - c0]`` of the sink gradient for batch entries
+    ``[batch_begin, batch_end)``; ``lse`` and ``delta`` hold those entries' rows only."""
+    dev = lse.device
+    n = (int(batch_end) - int(batch_begin)) * int(heads) * int(q_len)
+    for t, nm in ((lse, "lse"), (delta, "delta")):
+        if t.dtype != torch.float32 or t.numel() != n or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous float32 tensor of the shard's rows")
+    c0, c1 = sink_chunk_range(q_len, batch_begin, batch_end)
+    if partials is None:
+        partials = torch.empty((int(heads), max(0, c1 - c0)), dtype=torch.float32, device=dev)
+    if partials.dtype != torch.float32 or partials.numel() != heads * max(0, c1 - c0) or \
+            not partials.is_contiguous():
+        raise ValueError("partials must be a contiguous float32 tensor [heads, c1 - c0]")
+    for t, nm in ((lse, "lse"), (delta, "delta"), (sink, "sink"), (partials, "partials")):
+        _check_cuda(t, nm, dev)
+    if sink is None:
+        raise ValueError("sink is required")
+    rows = int(batch) * int(heads) * int(q_len)
+    d = _desc(rows, 1, 1, int(batch), int(heads), int(q_len), False, None, None, sink)
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_sink_grad_partials(ctypes.byref(d), int(batch_begin), int(batch_end),
+                                               _ptr(lse), _ptr(delta), _ptr(partials),
+                                               _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_sink_grad_partials")
+    return partials
+
+
+def fos_sink_grad_merge(partials):
+    """d_sink ``[heads]`` (CPU) from every shard's chunk partials, ``[heads, n_chunks]`` CPU
+    float32 in chunk order, added left to right by the library's host merge."""
+    if partials.is_cuda or partials.dtype != torch.float32 or partials.dim() != 2:
+        raise ValueError("partials must be a CPU float32 tensor [heads, n_chunks]")
+    partials = partials.contiguous()
+    heads, nchunks = partials.shape
+    out = torch.empty(heads, dtype=torch.float32)
+    st = _abi.lib().fos_sink_grad_merge(int(heads), int(nchunks), _ptr(partials), _ptr(out))
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_sink_grad_merge")
+    return out
+
+
 def _check_host(t, name):
     if t is not None and t.is_cuda:
         raise ValueError(f"{name} must be a host (CPU) tensor")

@@ -371,6 +371,53 @@ extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, cons
   return run_sink(desc, lse, delta, d_sink, stream, launch);
 }
 
+extern "C" fos_status fos_sink_grad_partials(const fos_desc *desc, int32_t batch_begin,
+                                             int32_t batch_end, const float *lse,
+                                             const float *delta, float *partials,
+                                             cudaStream_t stream, const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (desc->sink == nullptr || lse == nullptr || delta == nullptr || partials == nullptr)
+    return FOS_ERR_INVALID;
+  if (batch_begin < 0 || batch_end < batch_begin || batch_end > desc->batch)
+    return FOS_ERR_INVALID;
+  if (batch_end == batch_begin) return FOS_OK;  // an empty shard has no chunks
+  // the shard's positions [b0 * q_len, b1 * q_len) of every head must be whole chunks of the
+  // 256-position grid, except for a partial last chunk at the end of the batch
+  const int64_t p0 = (int64_t)batch_begin * desc->q_len, p1 = (int64_t)batch_end * desc->q_len;
+  if (p0 % kTileK != 0 || (batch_end < desc->batch && p1 % kTileK != 0)) return FOS_ERR_INVALID;
+  if (desc->heads == 0 || p1 == p0) return FOS_OK;
+  DevInfo *dev = nullptr;
+  if ((st = device_info(&dev)) != FOS_OK) return st;
+  SinkArgs a{};
+  a.batch = desc->batch;
+  a.heads = desc->heads;
+  a.q_len = desc->q_len;
+  a.sink = desc->sink;
+  a.lse = lse;
+  a.delta = delta;
+  const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
+  if (sink_partials_launch(a, batch_begin, batch_end, partials, warps * 32, stream) !=
+      cudaSuccess)
+    return FOS_ERR_CUDA;
+  return FOS_OK;
+}
+
+extern "C" fos_status fos_sink_grad_merge(int32_t heads, int64_t nchunks, const float *partials,
+                                          float *d_sink) {
+  if (heads < 0 || nchunks < 0) return FOS_ERR_INVALID;
+  if (heads > 0 && (d_sink == nullptr || (nchunks > 0 && partials == nullptr)))
+    return FOS_ERR_INVALID;
+  for (int32_t h = 0; h < heads; ++h) {
+    // float32 additions in chunk order from +0, as the device sum does
+    float total = 0.0f;
+    for (int64_t c = 0; c < nchunks; ++c) total = total + partials[(int64_t)h * nchunks + c];
+    d_sink[h] = total;
+  }
+  return FOS_OK;
+}
+
 extern "C" fos_status fos_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FOS_ERR_CUDA;
   unsigned v = 0;

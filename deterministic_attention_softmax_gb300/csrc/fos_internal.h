@@ -79,6 +79,9 @@ cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int 
                        size_t smem, cudaStream_t s);
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
+// Chunk partials of the batch entries [b0, b1) (arrays hold their rows from b0 * heads * q_len).
+cudaError_t sink_partials_launch(const SinkArgs &a, int64_t b0, int64_t b1, float *partials,
+                                 int threads, cudaStream_t s);
 
 // Host-side checks shared by the C ABI entry points (fos_api.cu).
 int dtype_size(fos_dtype dt);

@@ -11,12 +11,52 @@
 //   d_sink[h]  = chunk partials added left to right
 //
 // Warps take the chunks of one round in parallel; thread 0 adds the round's partials in
-// chunk order, so the result does not depend on the number of warps.
+// chunk order, so the result does not depend on the number of warps.  For rows sharded by
+// batch entry, fos_sink_partials_kernel writes the chunk partials of one shard instead; the
+// shards' partials, concatenated in chunk order and added left to right (fos_sink_grad_merge),
+// give these bits.
 #include "fos_device.cuh"
 #include "fos_internal.h"
 
 namespace fos {
 namespace {
+
+// Chunk c of head h (positions 256c .. 256c+255 of the head's rows in (b, i) order, those
+// below `pos_end`): the xor-tree sum of the lanes' ascending sums of c_r.  Rows are read at
+// r - row_base (the arrays may hold a range of rows that starts at row_base).
+__device__ __forceinline__ float sink_chunk(const SinkArgs &a, int h, float sk, int64_t c,
+                                            int64_t pos_end, int64_t row_base, int lane) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kLaneKeys; ++q) {
+    const int64_t p = c * kTileK + lane * kLaneKeys + q;
+    if (p < pos_end) {
+      const int64_t r = ((p / a.q_len) * a.heads + h) * a.q_len + (p % a.q_len) - row_base;
+      const float ps = (sk == -INFINITY) ? 0.0f : scale_fos(sk, a.lse[r]);
+      acc = __fadd_rn(acc, -__fmul_rn(ps, a.delta[r]));
+    }
+  }
+  return warp_sum_xor(acc);
+}
+
+// The chunk partials of one shard: batch entries [b0, b1), whose rows the arrays hold from row
+// b0 * heads * q_len on.  partials[h * (c1 - c0) + k] = chunk c0 + k of head h, where
+// [c0, c1) are the chunks of positions [b0 * q_len, b1 * q_len).
+__global__ void __launch_bounds__(1024) fos_sink_partials_kernel(const SinkArgs a, int64_t b0,
+                                                                 int64_t b1, float *partials) {
+  const int h = blockIdx.x;
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const int64_t p0 = b0 * a.q_len, p1 = b1 * a.q_len;
+  const int64_t c0 = p0 / kTileK, c1 = (p1 + kTileK - 1) / kTileK;
+  const int64_t row_base = b0 * a.heads * a.q_len;
+  const float sk = a.sink[h];
+  for (int64_t c = c0 + w; c < c1; c += nw) {
+    const float v = sink_chunk(a, h, sk, c, p1, row_base, lane);
+    if (lane == 0) partials[(int64_t)h * (c1 - c0) + (c - c0)] = v;
+  }
+}
 
 __global__ void __launch_bounds__(1024) fos_sink_kernel(const SinkArgs a) {
   __shared__ float part[32];
@@ -33,17 +73,7 @@ __global__ void __launch_bounds__(1024) fos_sink_kernel(const SinkArgs a) {
   for (int64_t base = 0; base < nchunks; base += nw) {
     const int64_t c = base + w;
     if (c < nchunks) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int q = 0; q < kLaneKeys; ++q) {
-        const int64_t p = c * kTileK + lane * kLaneKeys + q;
-        if (p < n) {
-          const int64_t r = ((p / a.q_len) * a.heads + h) * a.q_len + (p % a.q_len);
-          const float ps = (sk == -INFINITY) ? 0.0f : scale_fos(sk, a.lse[r]);
-          acc = __fadd_rn(acc, -__fmul_rn(ps, a.delta[r]));
-        }
-      }
-      acc = warp_sum_xor(acc);
+      const float acc = sink_chunk(a, h, sk, c, n, 0, lane);
       if (lane == 0) part[w] = acc;
     }
     __syncthreads();
@@ -59,6 +89,12 @@ __global__ void __launch_bounds__(1024) fos_sink_kernel(const SinkArgs a) {
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s) {
   fos_sink_kernel<<<a.heads, threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t sink_partials_launch(const SinkArgs &a, int64_t b0, int64_t b1, float *partials,
+                                 int threads, cudaStream_t s) {
+  fos_sink_partials_kernel<<<a.heads, threads, 0, s>>>(a, b0, b1, partials);
   return cudaGetLastError();
 }
 

@@ -158,6 +158,39 @@ fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *de
                          float *d_sink, cudaStream_t stream, const fos_launch *launch);
 
 /*
+ * The sink gradient with the rows sharded by batch entry (one shard per device, say): each
+ * shard writes the chunk partials of fos_sink_grad for its batch entries; the partials of all
+ * shards, concatenated per head in chunk order (shard order), go through fos_sink_grad_merge,
+ * which adds them left to right.  The result has the bits of fos_sink_grad on the whole batch,
+ * because each chunk's partial is the same sum and the final additions happen in the same
+ * order.  ("[ROCm] Jax Add softmax sink (learnable off-by-one) support": d_sink is a per-head
+ * sum over batch and query rows; here the cross-shard step is a gather, not an all-reduce,
+ * whose order would not be fixed.)
+ *   batch_begin, batch_end  the shard's batch entries [b0, b1), 0 <= b0 <= b1 <= batch (an
+ *                           empty shard is a no-op with no chunks); for a non-empty one the
+ *                           shard's positions [b0*q_len, b1*q_len) of a head must start on a
+ *                           multiple of 256 and end on one unless b1 == batch
+ *                           (FOS_ERR_INVALID otherwise)
+ *   lse, delta              device float [(b1-b0)*heads*q_len]: the shard's rows only
+ *   partials                device float [heads][c1 - c0] (output), c0 = b0*q_len/256,
+ *                           c1 = ceil(b1*q_len/256)
+ *   desc                    the whole problem (batch = all shards); desc->sink required
+ */
+fos_status fos_sink_grad_partials(const fos_desc *desc, int32_t batch_begin, int32_t batch_end,
+                                  const float *lse, const float *delta, float *partials,
+                                  cudaStream_t stream, const fos_launch *launch);
+
+/*
+ * d_sink[h] = +0 + partials[h][0] + partials[h][1] + ... in float32, left to right, on the
+ * host (no CUDA call): the merge of fos_sink_grad_partials' outputs.
+ *   partials  host float [heads][nchunks], every shard's chunks in order
+ *   d_sink    host float [heads] (output)
+ * FOS_ERR_INVALID for negative sizes or missing pointers; heads == 0 is a no-op.
+ */
+fos_status fos_sink_grad_merge(int32_t heads, int64_t nchunks, const float *partials,
+                               float *d_sink);
+
+/*
  * The forward, the backward and (when d_sink is given) the sink gradient of one batch whose
  * data live in HOST memory: the same results, bit for bit, as fos_softmax_fwd on a device
  * copy of scores, fos_softmax_bwd on the P it produced and dprobs, and fos_sink_grad, with

@@ -163,3 +163,60 @@ def test_step_host_refuses_before_any_cuda_call(abi):
     assert call(d, ws, need, dsink=FAKE) == abi.FOS_ERR_INVALID  # d_sink without a sink
     assert call(_desc(abi, rows=7), ws, need) == abi.FOS_ERR_INVALID
     assert call(_desc(abi, rows=0, batch=0), None, 0) == abi.FOS_OK  # empty: nothing enqueued
+
+
+def test_sink_grad_merge_adds_left_to_right_in_float32(abi):
+    import numpy as np
+
+    rng = np.random.default_rng(5)
+    parts = (rng.standard_normal((3, 37)) * 10.0 ** rng.integers(-6, 6, (3, 37))).astype(np.float32)
+    out = np.empty(3, dtype=np.float32)
+    st = abi.lib().fos_sink_grad_merge(3, 37, parts.ctypes.data_as(ctypes.c_void_p),
+                                       out.ctypes.data_as(ctypes.c_void_p))
+    assert st == abi.FOS_OK
+    for h in range(3):  # the same additions, one float32 rounding each
+        t = np.float32(0.0)
+        for c in range(37):
+            t = np.float32(t + parts[h, c])
+        assert out[h].tobytes() == t.tobytes()
+    lib = abi.lib()
+    assert lib.fos_sink_grad_merge(-1, 3, None, None) == abi.FOS_ERR_INVALID
+    assert lib.fos_sink_grad_merge(2, 3, None, out.ctypes.data_as(ctypes.c_void_p)) == abi.FOS_ERR_INVALID
+    assert lib.fos_sink_grad_merge(0, 3, None, None) == abi.FOS_OK
+    zero = np.full(2, 7.0, dtype=np.float32)  # no chunks: d_sink = +0
+    assert lib.fos_sink_grad_merge(2, 0, None, zero.ctypes.data_as(ctypes.c_void_p)) == abi.FOS_OK
+    assert zero.tobytes() == np.zeros(2, dtype=np.float32).tobytes()
+
+
+@pytest.mark.parametrize("b0,b1", [
+    (1, 4),    # starts at position 384: not on the 256 grid
+    (0, 1),    # ends at 384 and is not the last shard
+    (2, 1), (0, 5), (-1, 2),
+])
+def test_sink_grad_partials_refuses_misaligned_or_bad_shards(abi, b0, b1):
+    # refused before any CUDA call (never run a valid shard with these fake pointers)
+    d = _desc(abi, rows=4 * 3 * 384, batch=4, heads=3, q_len=384, ld=512, key_len=512, sink=FAKE)
+    st = abi.lib().fos_sink_grad_partials(ctypes.byref(d), b0, b1, FAKE, FAKE, FAKE, None, None)
+    assert st == abi.FOS_ERR_INVALID
+
+
+def test_sink_grad_partials_empty_shard_and_missing_sink(abi):
+    lib = abi.lib()
+    d = _desc(abi, rows=4 * 3 * 384, batch=4, heads=3, q_len=384, ld=512, key_len=512, sink=FAKE)
+    assert lib.fos_sink_grad_partials(ctypes.byref(d), 3, 3, FAKE, FAKE, FAKE, None, None) == abi.FOS_OK
+    nosink = _desc(abi, rows=4 * 3 * 384, batch=4, heads=3, q_len=384, ld=512, key_len=512)
+    assert lib.fos_sink_grad_partials(ctypes.byref(nosink), 0, 2, FAKE, FAKE, FAKE, None,
+                                      None) == abi.FOS_ERR_INVALID
+
+
+def test_batch_shards_start_on_the_chunk_grid():
+    from deterministic_attention_softmax_gb300.shard import batch_shards
+
+    for batch, q_len, parts in ((4, 384, 2), (4, 384, 3), (2, 2048, 2), (7, 100, 3), (64, 257, 4),
+                                (1, 16384, 2), (9, 256, 4)):
+        sh = batch_shards(batch, q_len, parts)
+        assert len(sh) == parts and sh[0][0] == 0 and sh[-1][1] == batch
+        for (a, b), (c, _) in zip(sh, sh[1:]):
+            assert b == c and a <= b
+        for a, b in sh:
+            assert a == b or (a * q_len) % 256 == 0

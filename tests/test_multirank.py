@@ -1,6 +1,6 @@
-"""The benchmark's multi-rank host logic on the CPU (world size 2, gloo): barrier, max and sum
-over ranks, and the reference arm running on rank 0 only.  Rows are independent, so ranks run
-replicas with no data-path exchange; this covers the timing and aggregation around them."""
+"""Multi-rank host logic on the CPU (world size 2, gloo): the benchmark's barrier, max and sum
+over ranks and its reference arm on rank 0 only; and the one cross-shard step of the path, the
+sink gradient's gather of per-shard chunk partials and their left-to-right merge."""
 
 import os
 import socket
@@ -73,3 +73,50 @@ def test_reference_arm_prints_one_line_on_a_single_rank():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def _sink_worker(rank, world, port, out):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    from deterministic_attention_softmax_gb300.shard import sharded_sink_grad
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        rng = np.random.default_rng(17)  # the same global partials on both ranks
+        full = (rng.standard_normal((3, 11)) * 10.0 ** rng.integers(-5, 5, (3, 11))).astype(np.float32)
+        cols = [(0, 5), (5, 11)][rank]  # rank 0 holds chunks 0..4, rank 1 chunks 5..10
+        mine = torch.from_numpy(np.ascontiguousarray(full[:, cols[0]:cols[1]]))
+        d = sharded_sink_grad(mine)
+        out.put((rank, d.numpy().tobytes(), full.tobytes()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_sink_grad_gathers_in_rank_order_and_merges_left_to_right():
+    import numpy as np
+
+    import deterministic_attention_softmax_gb300 as fos
+
+    fos.build()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_sink_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    full = np.frombuffer(res[0][2], dtype=np.float32).reshape(3, 11)
+    want = np.empty(3, dtype=np.float32)
+    for h in range(3):  # one float32 rounding per addition, chunks in order, from +0
+        t = np.float32(0.0)
+        for c in range(11):
+            t = np.float32(t + full[h, c])
+        want[h] = t
+    assert res[0][1] == want.tobytes() and res[1][1] == want.tobytes()
