@@ -92,7 +92,7 @@ fos_status check_launch(const fos_launch *l) {
   if (l->warps_per_cta < 0 || l->warps_per_cta > 16) return FOS_ERR_INVALID;
   if (l->ctas < 0) return FOS_ERR_INVALID;
   if (l->stages < 0 || l->stages > kMaxStages) return FOS_ERR_INVALID;
-  if (l->load_path < 0 || l->load_path > 2) return FOS_ERR_INVALID;
+  if (l->load_path < 0 || l->load_path > 3) return FOS_ERR_INVALID;
   if (l->wait_timeout_ns < 0) return FOS_ERR_INVALID;
   if (l->test_stall != 0 && l->test_stall != 1) return FOS_ERR_INVALID;
   if (l->generic != 0 && l->generic != 1) return FOS_ERR_INVALID;
@@ -140,22 +140,27 @@ struct Plan {
 
 // Fills the shared part of RowArgs and picks path, stages, CTAs.  `inputs` are the row
 // arrays that are staged (scores, or P and dP); `copies` is how many of them a stage holds.
+// seg_tiles > 0 plans a streaming kernel: stages hold segments of that many tiles (bulk
+// copies only), the statistics arrays still cover the whole row.
 template <typename OccFn>
 fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
                      const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
                      size_t (*extra)(int, int), int default_warps, size_t stage_target,
-                     uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl) {
+                     uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl, int seg_tiles = 0) {
   const int esz = dtype_size(dt);
   const int T = (d->key_len + kTileK - 1) / kTileK;
-  const size_t stage_bytes = (size_t)T * kTileK * esz;
+  const int stage_tiles = (seg_tiles > 0 && seg_tiles < T) ? seg_tiles : T;
+  const size_t stage_bytes = (size_t)stage_tiles * kTileK * esz;
   const bool stride16 = ((d->ld * esz) & 15) == 0;
   bool in_aligned = stride16;
   for (int i = 0; i < copies; ++i) in_aligned = in_aligned && aligned16(inputs[i]);
   const bool bulk_ok = in_aligned && (((int64_t)d->key_len * esz) & 15) == 0;
   const int path = l ? l->load_path : 0;
-  if (path == 1 && !bulk_ok) return FOS_ERR_UNSUPPORTED;
-  const bool bulk = (path == 1) || (path == 0 && bulk_ok);
+  const bool need_bulk = path == 1 || path == 3 || seg_tiles > 0;
+  if (need_bulk && !bulk_ok) return FOS_ERR_UNSUPPORTED;
+  if (seg_tiles > 0 && path == 2) return FOS_ERR_UNSUPPORTED;
+  const bool bulk = need_bulk || (path == 0 && bulk_ok);
 
   const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : default_warps;
   const int threads = (warps + 1) * 32;  // the compute warps and one producer warp
@@ -216,6 +221,7 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t 
   ra->T = T;
   ra->stages = stages;
   ra->stage_bytes = (uint32_t)stage_bytes;
+  ra->seg_tiles = seg_tiles > 0 ? stage_tiles : 0;
   ra->use_bulk = bulk ? 1 : 0;
   ra->in_vec = in_aligned ? 1 : 0;
   ra->out_vec = (stride16 && aligned16(output)) ? 1 : 0;
@@ -240,6 +246,19 @@ using namespace fos;
 
 namespace fos {
 
+// Rows longer than a shared-memory stage (or load_path 3): segments of this many tiles, read
+// twice, with this many compute warps by default.
+constexpr int kStreamSegTiles = 16;
+constexpr int kStreamWarps = 8;
+
+bool stream_rows(const fos_desc *desc, fos_dtype dtype, int copies, size_t (*extra)(int, int),
+                 const fos_launch *launch, const DevInfo &dev) {
+  if (launch && launch->load_path == 3) return true;
+  const int T = (desc->key_len + kTileK - 1) / kTileK;
+  const size_t whole = extra(T, 0) + (size_t)copies * T * kTileK * dtype_size(dtype);
+  return whole > (size_t)dev.max_smem;
+}
+
 fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
                    const void *scores, void *probs, float *lse, cudaStream_t stream,
                    const fos_launch *launch) {
@@ -250,6 +269,24 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   FwdArgs a{};
   Plan pl;
   const void *inputs[1] = {scores};
+  if (stream_rows(desc, dtype, 1, fwd_extra_smem, launch, *dev)) {
+    const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kStreamWarps;
+    st = plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev, fwd_extra_smem,
+                   warps, 24 * 1024, 0x300u | ((uint32_t)dtype << 4),
+                   [dtype](int th, size_t sm, int *n) {
+                     return fwd_stream_occupancy(dtype, th, sm, n);
+                   },
+                   &a, &pl, kStreamSegTiles);
+    if (st != FOS_OK) return st;
+    a.scores = scores;
+    a.probs = probs;
+    a.lse = lse;
+    a.sink = desc->sink;
+    if (desc->sink) a.need_geo = 1;
+    if (fwd_stream_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+    return FOS_OK;
+  }
   const int T = (desc->key_len + kTileK - 1) / kTileK;
   const int warps =
       (launch && launch->warps_per_cta) ? launch->warps_per_cta : fwd_default_warps(T);
@@ -291,6 +328,23 @@ fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   BwdArgs a{};
   Plan pl;
   const void *inputs[2] = {probs, dprobs};
+  if (stream_rows(desc, dtype, 2, bwd_extra_smem, launch, *dev)) {
+    const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kStreamWarps;
+    st = plan_rows(desc, dtype, row_base, nrows, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
+                   warps, 48 * 1024, 0x400u | ((uint32_t)dtype << 4),
+                   [dtype](int th, size_t sm, int *n) {
+                     return bwd_stream_occupancy(dtype, th, sm, n);
+                   },
+                   &a, &pl, kStreamSegTiles);
+    if (st != FOS_OK) return st;
+    a.probs = probs;
+    a.dprobs = dprobs;
+    a.dscores = dscores;
+    a.delta = delta;
+    if (bwd_stream_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+    return FOS_OK;
+  }
   const int esz = dtype_size(dtype);
   const bool fast = !(launch && launch->generic) && !(launch && launch->load_path == 2) &&
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask &&

@@ -88,6 +88,60 @@ __device__ __forceinline__ void tile_grad(const float (&p)[8], const float (&d)[
   }
 }
 
+// Pass 1 over the staged tiles tl = w, w + nw, ... < nt (a whole row, or one segment of it,
+// whose keys are numbered from 0 and valid below lim): the tile partials of delta into td[tl],
+// two tiles at a time.
+template <typename T>
+__device__ __forceinline__ void delta_partials(const unsigned char *sp, const unsigned char *sd,
+                                               int nt, int w, int nw, int lane, int lim,
+                                               const uint8_t *km, float *td) {
+  int t = w;
+  for (; t + nw < nt; t += 2 * nw) {
+    const int t1 = t + nw;
+    const int j0 = t * kTileK + lane * kLaneKeys, j1 = t1 * kTileK + lane * kLaneKeys;
+    float p0[8], d0[8], p1[8], d1[8];
+    tile_pdp<T>(sp, sd, j0, p0, d0);
+    tile_pdp<T>(sp, sd, j1, p1, d1);
+    const bool m0 = km != nullptr || (t + 1) * kTileK > lim;
+    const bool m1 = km != nullptr || (t1 + 1) * kTileK > lim;
+    float2 acc = (m0 || m1) ? make_float2(lane_dot(p0, d0, j0, lim, km, m0),
+                                          lane_dot(p1, d1, j1, lim, km, m1))
+                            : lane_dot2(p0, d0, p1, d1);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)  // the xor tree of both tiles, packed
+      acc = __fadd2_rn(acc, make_float2(__shfl_xor_sync(kFull, acc.x, o),
+                                        __shfl_xor_sync(kFull, acc.y, o)));
+    if (lane == 0) {
+      td[t] = acc.x;
+      td[t1] = acc.y;
+    }
+  }
+  if (t < nt) {
+    const int j0 = t * kTileK + lane * kLaneKeys;
+    float p0[8], d0[8];
+    tile_pdp<T>(sp, sd, j0, p0, d0);
+    const float a0 =
+        warp_sum_xor(lane_dot(p0, d0, j0, lim, km, km != nullptr || (t + 1) * kTileK > lim));
+    if (lane == 0) td[t] = a0;
+  }
+}
+
+// Pass 2 over the same staged tiles: dScores of tile tl written at tile t_base + tl of the row.
+template <typename T>
+__device__ __forceinline__ void grad_tiles(const unsigned char *sp, const unsigned char *sd,
+                                           int nt, int w, int nw, int lane, int lim,
+                                           const uint8_t *km, float delta, unsigned char *grow,
+                                           int t_base, int L, bool ovec) {
+  for (int t = w; t < nt; t += nw) {
+    const int j0 = t * kTileK + lane * kLaneKeys;
+    float p[8], d[8], v[8];
+    tile_pdp<T>(sp, sd, j0, p, d);
+    const bool masked = km != nullptr || (t + 1) * kTileK > lim;
+    tile_grad(p, d, j0, lim, km, masked, delta, v);
+    store_lane8<T>(grow, (t_base + t) * kTileK + lane * kLaneKeys, L, ovec, v);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
                                             int lim, bool vec, int nthreads) {
@@ -230,37 +284,7 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
     const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: tile partials of delta, two tiles at a time
-    {
-      int t = w;
-      for (; t + nw < Te; t += 2 * nw) {
-        const int t1 = t + nw;
-        const int j0 = t * kTileK + lane * kLaneKeys, j1 = t1 * kTileK + lane * kLaneKeys;
-        float p0[8], d0[8], p1[8], d1[8];
-        tile_pdp<T>(sp, sd, j0, p0, d0);
-        tile_pdp<T>(sp, sd, j1, p1, d1);
-        const bool m0 = km != nullptr || (t + 1) * kTileK > lim;
-        const bool m1 = km != nullptr || (t1 + 1) * kTileK > lim;
-        float2 acc = (m0 || m1) ? make_float2(lane_dot(p0, d0, j0, lim, km, m0),
-                                              lane_dot(p1, d1, j1, lim, km, m1))
-                                : lane_dot2(p0, d0, p1, d1);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)  // the xor tree of both tiles, packed
-          acc = __fadd2_rn(acc, make_float2(__shfl_xor_sync(kFull, acc.x, o),
-                                            __shfl_xor_sync(kFull, acc.y, o)));
-        if (lane == 0) {
-          td[t] = acc.x;
-          td[t1] = acc.y;
-        }
-      }
-      if (t < Te) {
-        const int j0 = t * kTileK + lane * kLaneKeys;
-        float p0[8], d0[8];
-        tile_pdp<T>(sp, sd, j0, p0, d0);
-        const float a0 =
-            warp_sum_xor(lane_dot(p0, d0, j0, lim, km, km != nullptr || (t + 1) * kTileK > lim));
-        if (lane == 0) td[t] = a0;
-      }
-    }
+    delta_partials<T>(sp, sd, Te, w, nw, lane, lim, km, td);
 
     if (compute_sync_or(ncomp, timed_out)) {
       if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
@@ -286,14 +310,7 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
     // ---- pass 2: dScores
     unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
     const bool ovec = kFast || a.out_vec != 0;
-    for (int t = w; t < Te; t += nw) {
-      const int j0 = t * kTileK + lane * kLaneKeys;
-      float p[8], d[8], v[8];
-      tile_pdp<T>(sp, sd, j0, p, d);
-      const bool masked = km != nullptr || (t + 1) * kTileK > lim;
-      tile_grad(p, d, j0, lim, km, masked, delta, v);
-      store_lane8<T>(grow, j0, a.L, ovec, v);
-    }
+    grad_tiles<T>(sp, sd, Te, w, nw, lane, lim, km, delta, grow, 0, a.L, ovec);
     if (use_bulk) {  // done with the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
@@ -305,6 +322,202 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
       store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
     }
   }
+}
+
+// ------------------------------------------------ rows longer than shared memory (streaming)
+//
+// As in the forward: a row too long to stage is read twice, in segments of a.seg_tiles tiles
+// of P and dP that cycle through the ring; pass 1 takes the tile partials of delta segment by
+// segment, one thread adds them left to right, and pass 2 reads every segment again for
+// dScores.  The per-tile arithmetic and the order of the delta sum are those of
+// fos_bwd_kernel, so a row gives the same bits on either path.
+
+// Producer: each row's segments of P and dP twice (pass 1, then pass 2), with the row's record
+// beside every segment; a row with no valid key still gets one empty segment per pass.
+template <typename T>
+__device__ void bwd_stream_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
+                                   uint64_t *full, uint64_t *empty, int4 *geos,
+                                   unsigned char *ring, size_t slot, bool stall) {
+  constexpr int esz = Io<T>::kEsz;
+  const int NS = a.stages;
+  const int seg_keys = a.seg_tiles * kTileK;
+  uint32_t issued = 0, last_ph = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int64_t n = 0;  // segments issued so far
+  bool stop = false;
+  for (int64_t kk = 0; kk < nmine && !stop; ++kk) {
+    const int64_t rr = r0 + kk * G;
+    const int4 g = row_geometry(a, rr);
+    const int nseg = g.x > 0 ? (g.x + seg_keys - 1) / seg_keys : 1;
+    const size_t off = (size_t)rr * a.ld * esz;
+    for (int pass = 0; pass < 2 && !stop; ++pass) {
+      for (int seg = 0; seg < nseg; ++seg, ++n) {
+        if (n >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, a.timeout_ns)) {
+          raise_device_error(a.err, kDevErrTimeout);
+          stop = true;
+          break;
+        }
+        const int k0 = seg * seg_keys;
+        const int nk = min(seg_keys, max(0, g.x - k0));
+        geos[s] = make_int4(g.x, g.y, g.z, seg);
+        const uint32_t bytes = ((uint32_t)nk * esz + 15u) & ~15u;  // never past the row
+        if (!(stall && n == 0)) {  // test only: the first copies are never issued
+          const uint32_t bar_a = smem_addr(&full[s]);
+          mbar_arrive_expect_tx(bar_a, 2u * bytes);
+          if (bytes) {
+            unsigned char *st = ring + (size_t)s * slot;
+            const size_t so = off + (size_t)k0 * esz;
+            bulk_g2s(smem_addr(st), static_cast<const unsigned char *>(a.probs) + so, bytes, bar_a);
+            bulk_g2s(smem_addr(st + a.stage_bytes),
+                     static_cast<const unsigned char *>(a.dprobs) + so, bytes, bar_a);
+          }
+          issued |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+        }
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+  for (int t = 0; t < NS; ++t)
+    if (issued & (1u << t))
+      mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
+template <typename T>
+__global__ void __maxnreg__(80) fos_bwd_stream_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + 16;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes);
+  unsigned char *ring = smem + kBarBytes + kGeoBytes;
+  const size_t slot = 2 * (size_t)a.stage_bytes;
+  float *td = reinterpret_cast<float *>(ring + (size_t)a.stages * slot);
+  float *dsm = td + ((a.T + 3) & ~3);
+
+  const int tid = threadIdx.x;
+  const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
+  const int ncomp = nw * 32;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t G = gridDim.x;
+  const int64_t r0 = blockIdx.x;
+  if (r0 >= a.rows) return;
+  const int64_t nmine = (a.rows - 1 - r0) / G + 1;
+  const int NS = a.stages;
+  const int SEG = a.seg_tiles;
+
+  if (tid == 0) {
+    for (int t = 0; t < NS; ++t) {
+      mbar_init(smem_addr(&full[t]), 1);
+      mbar_init(smem_addr(&empty[t]), nw);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (w == nw) {
+    if (lane == 0)
+      bwd_stream_produce<T>(a, r0, G, nmine, full, empty, geos, ring, slot,
+                            a.test_stall && blockIdx.x == 0);
+    return;
+  }
+
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * G;
+    bool timed_out = false;
+    int lim = 0, Te = 0, nseg = 1;
+    const uint8_t *km = nullptr;
+
+    // ---- pass 1: tile partials of delta, segment by segment
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns)) {
+        timed_out = true;
+        break;
+      }
+      if (seg == 0) {
+        const int4 g = geos[s];
+        lim = g.x;
+        Te = (lim + kTileK - 1) / kTileK;
+        nseg = Te > 0 ? (Te + SEG - 1) / SEG : 1;
+        km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+      }
+      const unsigned char *sp = ring + (size_t)s * slot;
+      const int t0 = seg * SEG;
+      delta_partials<T>(sp, sp + a.stage_bytes, min(SEG, Te - t0), w, nw, lane,
+                        lim - t0 * kTileK, km ? km + t0 * kTileK : nullptr, td + t0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (compute_sync_or(ncomp, timed_out)) {
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
+      return;
+    }
+
+    // ---- tile partials added left to right (one thread), as in fos_bwd_kernel
+    if (tid == 0) {
+      float delta = 0.0f;
+      int t = 0;
+      for (; t + 4 <= Te; t += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(td + t);
+        delta = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(delta, v.x), v.y), v.z), v.w);
+      }
+      for (; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
+      dsm[0] = delta;
+      if (a.delta) a.delta[r] = delta;
+    }
+    compute_sync(ncomp);
+    const float delta = dsm[0];
+
+    // ---- pass 2: every segment again, dScores
+    unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
+    const bool ovec = a.out_vec != 0;
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns)) {
+        timed_out = true;
+        break;
+      }
+      const unsigned char *sp = ring + (size_t)s * slot;
+      const int t0 = seg * SEG;
+      grad_tiles<T>(sp, sp + a.stage_bytes, min(SEG, Te - t0), w, nw, lane, lim - t0 * kTileK,
+                    km ? km + t0 * kTileK : nullptr, delta, grow, t0, a.L, ovec);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    for (int t = Te + w; t < a.T; t += nw) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+    // a wait that ran out in pass 2 stops every compute warp (none is left at a barrier)
+    if (compute_sync_or(ncomp, timed_out)) {
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
+      return;
+    }
+  }
+}
+
+const void *bwd_stream_fn(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_stream_kernel<float>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_stream_kernel<__nv_bfloat16>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_stream_kernel<__half>);
+  }
+  return nullptr;
 }
 
 template <bool kFast>
@@ -343,7 +556,19 @@ cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  return cudaFuncSetAttribute(bwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_smem);
+}
+
+cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, bwd_stream_fn(dt), threads,
+                                                       smem);
+}
+
+cudaError_t bwd_stream_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                              cudaStream_t s) {
+  void *args[] = {const_cast<BwdArgs *>(&a)};
+  return cudaLaunchKernel(bwd_stream_fn(dt), dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm) {

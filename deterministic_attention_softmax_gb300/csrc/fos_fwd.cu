@@ -141,6 +141,54 @@ __device__ __forceinline__ void tile_store(unsigned char *prow, int t, int lane,
   store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, L, ovec, v);
 }
 
+// Warp 0: fold the Te tile states left to right, starting from (M, S) = (sink, 1) or (-inf, 0)
+// (the prefix maxima and the rescale factors are formed lane-parallel, the fold itself is
+// sequential), then write the per-tile scales c_t = exp(m_t - M) / S to tc.  Every lane ends
+// with the final (M, S).  tc doubles as the fold's 64-float scratch.
+__device__ __forceinline__ void merge_tiles(int Te, int lane, const float *tm, const float *ts,
+                                            float *tc, float &M, float &S) {
+  for (int base = 0; base < Te; base += 32) {
+    const int t = base + lane;
+    const float mt = t < Te ? tm[t] : -INFINITY;
+    const float st = t < Te ? ts[t] : 0.0f;
+    float pm = mt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(kFull, pm, o);
+      if (lane >= o) pm = fmaxf(pm, y);
+    }
+    pm = fmaxf(pm, M);
+    float prev = __shfl_up_sync(kFull, pm, 1);
+    if (lane == 0) prev = M;
+    // flushing these factors cannot change S (see scale_ftz)
+    const float alpha = scale_ftz(prev, pm);
+    const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
+    // The fold itself is sequential: every lane reads the factors back from shared
+    // memory (broadcast 16-byte reads) and runs the same chain.  Slots past the last
+    // tile hold (1, 0), an exact no-op on S (S * 1 = S, S + 0 = S), so the chain always
+    // runs in steps of four.  tc doubles as the scratch: it is rewritten after the fold.
+    const int n = min(32, Te - base);
+    float *ab = tc;
+    ab[lane] = (lane < n) ? alpha : 1.0f;
+    ab[32 + lane] = (lane < n) ? beta : 0.0f;
+    __syncwarp();
+    for (int q0 = 0; q0 < n; q0 += 4) {
+      const float4 av = *reinterpret_cast<const float4 *>(ab + q0);
+      const float4 bv = *reinterpret_cast<const float4 *>(ab + 32 + q0);
+      S = __fadd_rn(__fmul_rn(S, av.x), bv.x);
+      S = __fadd_rn(__fmul_rn(S, av.y), bv.y);
+      S = __fadd_rn(__fmul_rn(S, av.z), bv.z);
+      S = __fadd_rn(__fmul_rn(S, av.w), bv.w);
+    }
+    __syncwarp();
+    M = __shfl_sync(kFull, pm, n - 1);
+  }
+  for (int t = lane; t < Te; t += 32) {
+    const float mt = tm[t];
+    tc[t] = (mt == -INFINITY) ? 0.0f : __fdiv_rn(scale_fos(mt, M), S);
+  }
+}
+
 // Copy keys [0, lim) of a row into the stage with plain loads (unaligned or forced path).
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
@@ -323,46 +371,7 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
         M = a.sink[g.z];
         S = 1.0f;
       }
-      for (int base = 0; base < Te; base += 32) {
-        const int t = base + lane;
-        const float mt = t < Te ? tm[t] : -INFINITY;
-        const float st = t < Te ? ts[t] : 0.0f;
-        float pm = mt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(kFull, pm, o);
-          if (lane >= o) pm = fmaxf(pm, y);
-        }
-        pm = fmaxf(pm, M);
-        float prev = __shfl_up_sync(kFull, pm, 1);
-        if (lane == 0) prev = M;
-        // flushing these factors cannot change S (see scale_ftz)
-        const float alpha = scale_ftz(prev, pm);
-        const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
-        // The fold itself is sequential: every lane reads the factors back from shared
-        // memory (broadcast 16-byte reads) and runs the same chain.  Slots past the last
-        // tile hold (1, 0), an exact no-op on S (S * 1 = S, S + 0 = S), so the chain always
-        // runs in steps of four.  tc doubles as the scratch: it is rewritten after the fold.
-        const int n = min(32, Te - base);
-        float *ab = tc;
-        ab[lane] = (lane < n) ? alpha : 1.0f;
-        ab[32 + lane] = (lane < n) ? beta : 0.0f;
-        __syncwarp();
-        for (int q0 = 0; q0 < n; q0 += 4) {
-          const float4 av = *reinterpret_cast<const float4 *>(ab + q0);
-          const float4 bv = *reinterpret_cast<const float4 *>(ab + 32 + q0);
-          S = __fadd_rn(__fmul_rn(S, av.x), bv.x);
-          S = __fadd_rn(__fmul_rn(S, av.y), bv.y);
-          S = __fadd_rn(__fmul_rn(S, av.z), bv.z);
-          S = __fadd_rn(__fmul_rn(S, av.w), bv.w);
-        }
-        __syncwarp();
-        M = __shfl_sync(kFull, pm, n - 1);
-      }
-      for (int t = lane; t < Te; t += 32) {
-        const float mt = tm[t];
-        tc[t] = (mt == -INFINITY) ? 0.0f : __fdiv_rn(scale_fos(mt, M), S);
-      }
+      merge_tiles(Te, lane, tm, ts, tc, M, S);
     }
     compute_sync(ncomp);
     if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
@@ -402,6 +411,215 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
     // Tile t's tm entry is written (pass 1) and re-read (pass 2) by warp t % nw only, and tc
     // is rewritten after the next row's first barrier: no barrier is needed here.
   }
+}
+
+// ------------------------------------------------ rows longer than shared memory (streaming)
+//
+// A row whose staged copy would not fit in shared memory is read twice, in segments of
+// a.seg_tiles tiles that cycle through the same ring: pass 1 takes the tile statistics
+// segment by segment, the merge is the one above, and pass 2 reads every segment again and
+// recomputes e_j from the stored tile maxima, as the staged kernel's recompute mode does.  The
+// per-tile arithmetic and the merge are those of fos_fwd_kernel, so a row gives the same bits
+// on either path; the price is a second read of the scores.
+
+// Producer: each row's segments twice (pass 1, then pass 2), in order through the ring, with
+// the row's record {limit, batch entry, head, segment} beside every segment.  A row with no
+// valid key still gets one (empty) segment per pass, so its record reaches the compute warps.
+template <typename T>
+__device__ void fwd_stream_produce(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
+                                   uint64_t *full, uint64_t *empty, int4 *geos,
+                                   unsigned char *ring, bool stall) {
+  constexpr int esz = Io<T>::kEsz;
+  const int NS = a.stages;
+  const int seg_keys = a.seg_tiles * kTileK;
+  uint32_t issued = 0, last_ph = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int64_t n = 0;  // segments issued so far
+  bool stop = false;
+  for (int64_t kk = 0; kk < nmine && !stop; ++kk) {
+    const int64_t rr = r0 + kk * G;
+    const int4 g = row_geometry(a, rr);
+    const int nseg = g.x > 0 ? (g.x + seg_keys - 1) / seg_keys : 1;
+    const unsigned char *src = static_cast<const unsigned char *>(a.scores) + (size_t)rr * a.ld * esz;
+    for (int pass = 0; pass < 2 && !stop; ++pass) {
+      for (int seg = 0; seg < nseg; ++seg, ++n) {
+        if (n >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, a.timeout_ns)) {
+          raise_device_error(a.err, kDevErrTimeout);
+          stop = true;
+          break;
+        }
+        const int k0 = seg * seg_keys;
+        const int nk = min(seg_keys, max(0, g.x - k0));
+        geos[s] = make_int4(g.x, g.y, g.z, seg);
+        // rounded up to 16 bytes; never past the row since L * esz is a multiple of 16 here
+        const uint32_t bytes = ((uint32_t)nk * esz + 15u) & ~15u;
+        if (!(stall && n == 0)) {  // test only: the first copy is never issued
+          const uint32_t bar_a = smem_addr(&full[s]);
+          mbar_arrive_expect_tx(bar_a, bytes);
+          if (bytes) bulk_g2s(smem_addr(ring + (size_t)s * a.stage_bytes), src + (size_t)k0 * esz,
+                              bytes, bar_a);
+          issued |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+        }
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+  for (int t = 0; t < NS; ++t)
+    if (issued & (1u << t))
+      mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
+template <typename T>
+__global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + 16;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes);
+  unsigned char *ring = smem + kBarBytes + kGeoBytes;
+  const int T4 = (a.T + 3) & ~3;
+  float *tm = reinterpret_cast<float *>(ring + (size_t)a.stages * a.stage_bytes);
+  float *ts = tm + T4;
+  float *tc = ts + T4;
+
+  const int tid = threadIdx.x;
+  const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
+  const int ncomp = nw * 32;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t G = gridDim.x;
+  const int64_t r0 = blockIdx.x;
+  if (r0 >= a.rows) return;
+  const int64_t nmine = (a.rows - 1 - r0) / G + 1;
+  const int NS = a.stages;
+  const int SEG = a.seg_tiles;
+
+  if (tid == 0) {
+    for (int t = 0; t < NS; ++t) {
+      mbar_init(smem_addr(&full[t]), 1);
+      mbar_init(smem_addr(&empty[t]), nw);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (w == nw) {
+    if (lane == 0)
+      fwd_stream_produce<T>(a, r0, G, nmine, full, empty, geos, ring,
+                            a.test_stall && blockIdx.x == 0);
+    return;
+  }
+
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * G;
+    bool timed_out = false;
+    int4 g = make_int4(0, 0, 0, 0);
+    int lim = 0, Te = 0, nseg = 1;
+    const uint8_t *km = nullptr;
+
+    // ---- pass 1: tile statistics, segment by segment
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns)) {
+        timed_out = true;
+        break;
+      }
+      if (seg == 0) {
+        g = geos[s];
+        lim = g.x;
+        Te = (lim + kTileK - 1) / kTileK;
+        nseg = Te > 0 ? (Te + SEG - 1) / SEG : 1;
+        km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+      }
+      const unsigned char *stage = ring + (size_t)s * a.stage_bytes;
+      const int t0 = seg * SEG, nt = min(SEG, Te - t0);
+      const int lim_l = lim - t0 * kTileK;  // the segment's keys are numbered from 0
+      const uint8_t *kms = km ? km + t0 * kTileK : nullptr;
+      int tl = w;
+      for (; tl + nw < nt; tl += 2 * nw) {
+        float e0[8], e1[8];
+        tile_stats2<T>(stage, tl, tl + nw, lane, lim_l, kms, e0, e1, tm + t0, ts + t0);
+      }
+      if (tl < nt) {
+        float e0[8];
+        tile_stats1<T>(stage, tl, lane, lim_l, kms, e0, tm + t0, ts + t0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (compute_sync_or(ncomp, timed_out)) {
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
+      return;
+    }
+
+    // ---- merge (warp 0)
+    float M = -INFINITY, S = 0.0f;
+    if (w == 0) {
+      if (a.sink != nullptr) {
+        M = a.sink[g.z];
+        S = 1.0f;
+      }
+      merge_tiles(Te, lane, tm, ts, tc, M, S);
+    }
+    compute_sync(ncomp);
+    if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
+
+    // ---- pass 2: every segment again, e_j recomputed, P written
+    unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
+    const bool ovec = a.out_vec != 0;
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns)) {
+        timed_out = true;
+        break;
+      }
+      const unsigned char *stage = ring + (size_t)s * a.stage_bytes;
+      const int t0 = seg * SEG, nt = min(SEG, Te - t0);
+      const int lim_l = lim - t0 * kTileK;
+      const uint8_t *kms = km ? km + t0 * kTileK : nullptr;
+      for (int tl = w; tl < nt; tl += nw) {
+        float ee[8];
+        tile_exp<T>(stage, tl, lane, lim_l, kms, tm[t0 + tl], ee);
+        tile_store<T>(prow, t0 + tl, lane, a.L, ovec, ee, tc[t0 + tl]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    for (int t = Te + w; t < a.T; t += nw) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+    // a wait that ran out in pass 2 stops every compute warp (none is left at a barrier)
+    if (compute_sync_or(ncomp, timed_out)) {
+      if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
+      return;
+    }
+    // Each warp writes (pass 1) and reads (pass 2) the tm entries of its own tiles only, and tc
+    // is rewritten after the next row's first barrier.
+  }
+}
+
+const void *fwd_stream_fn(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_fwd_stream_kernel<float>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_fwd_stream_kernel<__nv_bfloat16>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_fwd_stream_kernel<__half>);
+  }
+  return nullptr;
 }
 
 template <int KT, bool kFast>
@@ -468,7 +686,19 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
       if (e != cudaSuccess) return e;
     }
-  return cudaSuccess;
+  return cudaFuncSetAttribute(fwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              max_smem);
+}
+
+cudaError_t fwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_stream_fn(dt), threads,
+                                                       smem);
+}
+
+cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int threads, size_t smem,
+                              cudaStream_t s) {
+  void *args[] = {const_cast<FwdArgs *>(&a)};
+  return cudaLaunchKernel(fwd_stream_fn(dt), dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,

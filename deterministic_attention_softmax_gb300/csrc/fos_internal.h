@@ -22,8 +22,10 @@ struct RowArgs {
   const int32_t *kv_valid_len; // [batch] or null
   const uint8_t *key_mask;     // [batch * L] or null
   int32_t T;                   // tiles per row, ceil(L / 256)
-  int32_t stages;              // rows in flight per CTA (bulk-copy path); 1 on the plain path
-  uint32_t stage_bytes;        // shared-memory bytes of one staged input row (T * 256 * esz)
+  int32_t stages;              // rows (or row segments) in flight per CTA; 1 on the plain path
+  uint32_t stage_bytes;        // shared-memory bytes of one stage: T * 256 * esz for a whole
+                               // row, seg_tiles * 256 * esz for the streaming kernels
+  int32_t seg_tiles;           // streaming kernels: tiles per segment (0: whole rows)
   int32_t use_bulk;            // 1: 1-D bulk copies (TMA) into the ring; 0: plain loads
   int32_t in_vec;              // input rows start 16-byte aligned
   int32_t out_vec;             // output rows start 16-byte aligned
@@ -72,11 +74,18 @@ cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t s
                           int *blocks_per_sm);
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
+// Rows longer than shared memory: segments of a.seg_tiles tiles, each read twice.
+cudaError_t fwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int threads, size_t smem,
+                              cudaStream_t s);
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
+cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t bwd_stream_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                              cudaStream_t s);
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
 // Chunk partials of the batch entries [b0, b1) (arrays hold their rows from b0 * heads * q_len).

@@ -1,12 +1,12 @@
-"""Seeded synthetic inputs for the five workloads (no softmax arithmetic in here).
+"""Seeded synthetic inputs for the workloads (no softmax arithmetic in here).
 
 Shared by the benchmark, the smoke check and the tests, on both sides of a parity check: the
 CUDA path and the oracle always receive the same tensor values (generated here, then copied to
 the host for the oracle).  Shapes and distributions follow the workloads the pages measure
 (Qwen-Image joint attention: 16,384 rows of 4,096 image + 256 text keys, "[WS1][kernels] Add
-fixed-order joint-attention softmax for Qwen-Image", Benchmark), with the padding, sink and
-large cases of the build's workload table.  No public dataset is involved; every value is
-drawn from a seeded normal or uniform distribution.
+fixed-order joint-attention softmax for Qwen-Image", Benchmark), plus padded prompts, causal
+rows with a sink, long bf16 / fp32 rows, and rows longer than a shared-memory stage.  No public
+dataset is involved; every value is drawn from a seeded normal or uniform distribution.
 """
 
 from __future__ import annotations
@@ -58,6 +58,8 @@ WORKLOADS = {
                  causal=True, sink=True),
         Workload("large_bf16", torch.bfloat16, 1, 24, 8192, 8192, 5.0, seed=4),
         Workload("large_fp32", torch.float32, 1, 24, 8192, 8192, 5.0, seed=4),
+        # rows longer than a shared-memory stage (262,144 keys): the streaming kernels
+        Workload("long_rows_bf16", torch.bfloat16, 1, 8, 128, 262144, 4.0, seed=5),
     )
 }
 

@@ -1,7 +1,6 @@
 """Parity tolerances between the CUDA library and the FP64 oracle -- TEST INFRASTRUCTURE ONLY.
 
-The bounds are the stated correctness bar of this build, read as follows (each reading is
-listed with its reason in the design notes):
+The bounds are the stated correctness bar of the kernels, read as follows:
 
 * P, float32 I/O: max |gpu - ref| <= 1e-6.
 * P, bf16/fp16 I/O: |gpu - ref| <= 1 ULP of the I/O dtype at the FP64 value.

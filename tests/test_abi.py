@@ -93,7 +93,7 @@ def test_rejects_null_pointers_and_bad_dtype(abi):
 
 @pytest.mark.parametrize("bad", [
     dict(warps_per_cta=17), dict(warps_per_cta=-1), dict(ctas=-2), dict(stages=17),
-    dict(load_path=3), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(generic=2),
+    dict(load_path=4), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(generic=2),
 ])
 def test_rejects_bad_launch_options(abi, bad):
     opts = dict(warps_per_cta=0, ctas=0, stages=0, load_path=0, wait_timeout_ns=0, test_stall=0,

@@ -21,12 +21,13 @@ def inputs(dtype=torch.bfloat16, rows=600, L=2048):
 
 
 @pytest.mark.parametrize("which", ["fwd", "bwd"])
-def test_stalled_copy_times_out_and_context_survives(which):
+@pytest.mark.parametrize("path", [1, 3])  # staged rows, streamed segments
+def test_stalled_copy_times_out_and_context_survives(which, path):
     x, dp = inputs()
     ref_p, ref_lse = fos.fos_softmax_fwd(x)
     ref_ds, ref_delta = fos.fos_softmax_bwd(ref_p, dp)
     assert fos.fos_device_error() == 0
-    stall = fos.Launch(test_stall=1, wait_timeout_ns=20_000_000, load_path=1)
+    stall = fos.Launch(test_stall=1, wait_timeout_ns=20_000_000, load_path=path)
     if which == "fwd":
         fos.fos_softmax_fwd(x, launch=stall)
     else:

@@ -1,6 +1,6 @@
 """GPU vs FP64 oracle, element by element, on small problems that span several tiles and a
 ragged tail, for every I/O dtype and mask kind, plus the edge cases (one key, fully masked
-rows, -inf sinks, long rows past the register path, the longest supported rows, unaligned
+rows, -inf sinks, long rows past the register path, the longest staged rows, unaligned
 rows, in-place calls).  All calls go through the C ABI."""
 
 import math
@@ -112,18 +112,6 @@ def test_longest_rows(dtype_name, L_fwd, L_bwd):
     ds, delta = fos.fos_softmax_bwd(p_in, c["dp"], batch=1, heads=1, q_len=2)
     ds_ref, delta_ref = oracle.softmax_bwd(np64(p_in), np64(c["dp"]), batch=1, heads=1, q_len=2)
     check_bwd(ds, delta, ds_ref, delta_ref, np64(p_in), np64(c["dp"]), dtype_name)
-
-
-@pytest.mark.parametrize("dtype_name", list(DTYPES))
-def test_rows_longer_than_shared_memory_are_refused(dtype_name):
-    dt = DTYPES[dtype_name]
-    x = torch.zeros(2, 400000, dtype=dt, device=dev())
-    with pytest.raises(fos.FosError) as e:
-        fos.fos_softmax_fwd(x)
-    assert e.value.status == 2  # FOS_ERR_UNSUPPORTED
-    with pytest.raises(fos.FosError) as e:
-        fos.fos_softmax_bwd(x, x)
-    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("dtype_name", list(DTYPES))

@@ -47,7 +47,7 @@ def test_workload_every_row(name):
 
 
 @pytest.mark.parametrize("name", ["prompt_padding_bf16", "sink_causal_bf16", "large_bf16",
-                                  "large_fp32"])
+                                  "large_fp32", "long_rows_bf16"])
 def test_workload_sampled_rows(name):
     w = W.WORKLOADS[name]
     d = dev()
