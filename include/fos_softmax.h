@@ -16,6 +16,12 @@
  * ld-1 are never read or written.  LSE and delta are float32 [rows]; sink and d_sink are
  * float32 [heads].
  *
+ * Long rows.  A row is normally staged whole in shared memory (up to about 57k fp32 / 113k
+ * bf16 keys forward, half that backward).  Longer rows are read twice, in segments of 16
+ * tiles, by streaming kernels with the same per-tile arithmetic and merge order, so a row gives
+ * the same bits either way; they need 16-byte aligned rows (base, ld * size and key_len * size
+ * multiples of 16 bytes) and fit up to about 4.5 M (forward) / 14 M (backward) bf16 keys.
+ *
  * Masks.  Key j of row r is valid iff all of the given conditions hold:
  *   causal:        j <= key_len - q_len + i
  *                  ("Batch-invariant attention", Prefill / Decode / KV-cache Contract)
@@ -50,8 +56,10 @@
  *   FOS_ERR_INVALID      bad arguments (null required pointer, rows != batch*heads*q_len,
  *                        key_len < 1, ld < key_len, unknown dtype, causal with q_len >
  *                        key_len, bad launch options); nothing is launched.
- *   FOS_ERR_UNSUPPORTED  valid, but beyond what the kernels stage (a row longer than shared
- *                        memory, or a forced load path the buffers do not allow).
+ *   FOS_ERR_UNSUPPORTED  valid, but beyond what the kernels take (a row too long to stage
+ *                        whose buffers do not allow bulk copies, a row whose tile statistics
+ *                        exceed shared memory, or a forced load path the buffers do not
+ *                        allow).
  *   FOS_ERR_CUDA         the launch failed (cudaGetLastError after the launch).
  *   FOS_ERR_TIMEOUT      reported by fos_device_error(): a bounded wait inside a kernel ran
  *                        out, the kernel stopped early and its outputs are not valid.
@@ -107,7 +115,9 @@ typedef struct fos_launch {
   int32_t warps_per_cta; /* 0 = default (chosen from key_len); otherwise 1..16 */
   int32_t ctas;          /* 0 = default (persistent: SMs x resident CTAs); else >= 1 */
   int32_t stages;        /* 0 = default; rows in flight per CTA on the bulk-copy path, 1..16 */
-  int32_t load_path;     /* 0 = auto, 1 = bulk copy (TMA) only, 2 = plain loads only */
+  int32_t load_path;     /* 0 = auto, 1 = bulk copy (TMA) only, 2 = plain loads only,
+                            3 = streaming: the row read twice in segments (the path taken
+                            anyway by rows too long to stage; same bits) */
   int64_t wait_timeout_ns; /* 0 = default (2 s): limit of every bounded wait in a kernel */
   int32_t test_stall;    /* 0; 1 = CTA 0 waits on a copy that is never issued (test only) */
   int32_t generic;       /* 0 = auto; 1 = never the kernel specialised for the common case */
