@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--warm-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["fwd", "bwd", "sink"], default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
@@ -175,6 +176,33 @@ def kernel_source_hash():
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def hbm_probe(dev, nbytes=1 << 30, reps=5):
+    """Attained HBM bandwidth on this device, now: a copy of 1 GiB of bf16 (read + write bytes),
+    best of `reps`, CUDA events.  Context for the roofline's measured peak, which another run on
+    another device of the same kind wrote."""
+    import torch
+
+    a = torch.ones(nbytes // 2, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+
+    def best(f):
+        f()
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return min(t)
+
+    copy_ms = best(lambda: b.copy_(a))
+    del a, b
+    return {"copy_gbs": 2 * nbytes / (copy_ms * 1e-3) / 1e9,
+            "how": f"torch copy_ of 1 GiB bf16 on this device (read + write bytes), best of {reps}"}
 
 
 def measured_peaks():
@@ -422,6 +450,30 @@ def run_ours(args):
                 "traffic": ncu_traffic(dom, w.name),
                 "algorithmic_bytes_per_launch": b["bwd"] if dom == "fos_bwd_kernel" else b["fwd"]}
 
+    # ---- warm variant: one input set reused every step, so L2 keeps what it can between
+    # the steps (the value above rotates sets larger than L2: the cold number)
+    warm = None
+    if args.warm_steps > 0:
+        wev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(args.warm_steps)]
+        for _ in range(3):
+            step(0)
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        w0.record(stream)
+        for i in range(args.warm_steps):
+            step(0, wev[i])
+        w1.record(stream)
+        torch.cuda.synchronize()
+        wms = w0.elapsed_time(w1) / args.warm_steps
+        wf = statistics.mean(e[0].elapsed_time(e[1]) for e in wev)
+        wb = statistics.mean(e[1].elapsed_time(e[2]) for e in wev)
+        warm = {"value": step_bytes / (wms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": wms,
+                "fwd_gbs": b["fwd"] / (wf * 1e-3) / 1e9, "bwd_gbs": b["bwd"] / (wb * 1e-3) / 1e9,
+                "steps": args.warm_steps, "inputs": f"one set of {set_bytes / 1e9:.2f} GB reused"}
+        assert fos.fos_device_error() == 0
+    p0 = hbm_probe(dev)
+
     # ---- end to end through the public Python API with pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
@@ -490,6 +542,7 @@ def run_ours(args):
         "rows_per_s_fwd_bwd": w.rows / (ms_step * 1e-3) * world,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch * K,
         "clocks": clocks, "parity_gate": "sampled rows vs FP64 oracle: pass",
+        "warm": warm, "p0_hbm_probe": p0,
     }
     print(json.dumps(line))
 
