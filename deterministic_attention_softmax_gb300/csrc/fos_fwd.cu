@@ -622,6 +622,155 @@ const void *fwd_stream_fn(fos_dtype dt) {
   return nullptr;
 }
 
+// ------------------------------------------------------ short rows: one warp per row
+//
+// A row of at most KT (<= 8) tiles is taken by one warp alone: it waits for the row's copy,
+// runs pass 1 on all its tiles (pairs of neighbouring tiles), folds the tile states with the
+// same merge, and writes P from the e_j it kept in registers.  No barrier joins the warps of a
+// CTA, so the merge of one row does not idle the others.  Each warp keeps its own ring of
+// a.stages row buffers and its lane 0 issues its own copies: the copy of row k + stages goes into
+// the buffer of row k as soon as pass 1 of row k has read it.  The per-tile arithmetic, the
+// merge and pass 2 are those of fos_fwd_kernel, so a row gives the same bits on either kernel.
+
+// Lane 0: the geometry of row rr into *geo and its bulk copy into `stage` on barrier `bar`.
+template <typename T>
+__device__ __forceinline__ void rw_issue(const FwdArgs &a, int64_t rr, unsigned char *stage,
+                                         uint64_t *bar, int4 *geo) {
+  constexpr int esz = Io<T>::kEsz;
+  const int4 g = row_geometry(a, rr);
+  *geo = g;
+  const uint32_t bytes = ((uint32_t)g.x * esz + 15u) & ~15u;  // never past the row
+  const uint32_t bar_a = smem_addr(bar);
+  fence_proxy_async_smem();  // the warp's reads of this buffer come before the copy
+  mbar_arrive_expect_tx(bar_a, bytes);
+  if (bytes)
+    bulk_g2s(smem_addr(stage),
+             static_cast<const unsigned char *>(a.scores) + (size_t)rr * a.ld * esz, bytes,
+             bar_a);
+}
+
+template <typename T, int KT>
+__global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp_kernel(
+    const FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  constexpr int kStat = 80;  // floats per warp: tm[8], ts[8], tc[64] (tc is the merge scratch)
+  const int nw = blockDim.x >> 5;
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NS = a.stages;  // row buffers per warp
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem) + w * NS;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes) + w * NS;
+  unsigned char *ring = smem + kBarBytes + kGeoBytes + (size_t)w * NS * a.stage_bytes;
+  float *tm = reinterpret_cast<float *>(smem + kBarBytes + kGeoBytes +
+                                        (size_t)nw * NS * a.stage_bytes) + w * kStat;
+  float *ts = tm + 8;
+  float *tc = tm + 16;
+
+  const int64_t GW = (int64_t)gridDim.x * nw;           // warps in the grid
+  const int64_t r0 = (int64_t)blockIdx.x * nw + w;        // this warp's first row
+  const int64_t nmine = r0 < a.rows ? (a.rows - 1 - r0) / GW + 1 : 0;
+  const bool stall = a.test_stall && blockIdx.x == 0 && w == 0;
+
+  if (lane == 0) {
+    for (int t = 0; t < NS; ++t) mbar_init(smem_addr(&full[t]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // prologue: the first rows' copies (test only: the very first one is never issued)
+  uint32_t issued = 0, last_ph = 0;
+  if (lane == 0)
+    for (int t = 0; t < NS && t < nmine; ++t)
+      if (!(stall && t == 0)) {
+        rw_issue<T>(a, r0 + t * GW, ring + (size_t)t * a.stage_bytes, &full[t], &geos[t]);
+        issued |= 1u << t;
+      }
+
+  int s = 0;
+  uint32_t ph = 0;
+  bool ok = true;
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * GW;
+    unsigned char *stage = ring + (size_t)s * a.stage_bytes;
+    // every lane waits; the warp stops as one if any lane's wait ran out
+    const bool landed = mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
+    if (!__all_sync(kFull, landed)) {
+      if (lane == 0) raise_device_error(a.err, kDevErrTimeout);
+      ok = false;
+      break;
+    }
+    const int4 g = geos[s];
+    const int lim = g.x;
+    const int Te = (lim + kTileK - 1) / kTileK;
+    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+
+    // ---- pass 1: every tile of the row, two neighbouring tiles at a time
+    float e[KT][8];
+#pragma unroll
+    for (int kk = 0; kk < KT; kk += 2) {
+      if (kk + 1 < Te)
+        tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e[kk], e[kk + 1], tm, ts);
+      else if (kk < Te)
+        tile_stats1<T>(stage, kk, lane, lim, km, e[kk], tm, ts);
+    }
+    __syncwarp();  // tm / ts (lane 0) for the merge; every lane is done with the buffer
+    if (lane == 0 && k + NS < nmine) {
+      rw_issue<T>(a, r + NS * GW, stage, &full[s], &geos[s]);
+      issued |= 1u << s;
+      last_ph = (last_ph & ~(1u << s)) | ((ph ^ 1u) << s);
+    }
+
+    // ---- merge (this warp)
+    float M = -INFINITY, S = 0.0f;
+    if (a.sink != nullptr) {
+      M = a.sink[g.z];
+      S = 1.0f;
+    }
+    merge_tiles(Te, lane, tm, ts, tc, M, S);
+    __syncwarp();  // tc
+    if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
+
+    // ---- pass 2: P from the e_j kept in registers
+    unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
+    const bool ovec = a.out_vec != 0;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk)
+      if (kk < Te) tile_store<T>(prow, kk, lane, a.L, ovec, e[kk], tc[kk]);
+    for (int t = Te; t < a.T; ++t) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+    __syncwarp();  // tc and tm / ts are rewritten by the next row
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  // every copy this warp issued has landed before it exits (its buffers stay allocated until
+  // the whole CTA is done, but no copy may outlive the CTA)
+  if (!ok && lane == 0)
+    for (int t = 0; t < NS; ++t)
+      if (issued & (1u << t))
+        mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
+template <int KT>
+const void *fwd_rowwarp_fn_kt(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_fwd_rowwarp_kernel<float, KT>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_fwd_rowwarp_kernel<__nv_bfloat16, KT>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_fwd_rowwarp_kernel<__half, KT>);
+  }
+  return nullptr;
+}
+
+const void *fwd_rowwarp_fn(fos_dtype dt, int kt) {
+  return kt <= 2 ? fwd_rowwarp_fn_kt<2>(dt) : (kt <= 4 ? fwd_rowwarp_fn_kt<4>(dt)
+                                                        : fwd_rowwarp_fn_kt<8>(dt));
+}
+
 template <int KT, bool kFast>
 const void *fwd_fn_kt(fos_dtype dt) {
   switch (dt) {
@@ -686,8 +835,30 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
       if (e != cudaSuccess) return e;
     }
+  for (int kt : {2, 4, 8}) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_rowwarp_fn(dt, kt),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncSetAttribute(fwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_smem);
+}
+
+cudaError_t fwd_rowwarp_occupancy(fos_dtype dt, int kt, int threads, size_t smem,
+                                  int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_rowwarp_fn(dt, kt),
+                                                       threads, smem);
+}
+
+cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
+                               size_t smem, cudaStream_t s) {
+  void *args[] = {const_cast<FwdArgs *>(&a)};
+  return cudaLaunchKernel(fwd_rowwarp_fn(dt, kt), dim3(grid), dim3(threads), args, smem, s);
+}
+
+size_t fwd_rowwarp_smem(int warps, int stages, size_t stage_bytes) {
+  return (size_t)kBarBytes + kGeoBytes + (size_t)warps * stages * stage_bytes +
+         (size_t)warps * 80 * sizeof(float);
 }
 
 cudaError_t fwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {

@@ -74,6 +74,13 @@ cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t s
                           int *blocks_per_sm);
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
+// Rows of at most 8 tiles, one warp per row: kt = 2, 4 or 8 tiles kept in registers; `warps`
+// warps per CTA, each with a.stages row buffers of a.stage_bytes.
+size_t fwd_rowwarp_smem(int warps, int stages, size_t stage_bytes);
+cudaError_t fwd_rowwarp_occupancy(fos_dtype dt, int kt, int threads, size_t smem,
+                                  int *blocks_per_sm);
+cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
+                               size_t smem, cudaStream_t s);
 // Rows longer than shared memory: segments of a.seg_tiles tiles, each read twice.
 cudaError_t fwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int threads, size_t smem,
