@@ -324,6 +324,137 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
   }
 }
 
+// ------------------------------------------------------ short rows: one warp per row
+//
+// As in the forward, a row of at most 8 tiles is taken by one warp alone: pass 1 (tile
+// partials of delta), the left-to-right sum of the partials (every lane adds them in the same
+// order, so no thread has to broadcast delta) and pass 2 (dScores), with no barrier between
+// the warps of a CTA.  Each warp keeps its own ring of a.stages buffers (P and dP of a row) and
+// its lane 0 refills a buffer with the copies of row k + stages once pass 2 of row k is done.
+// The per-tile arithmetic and the order of the delta sum are fos_bwd_kernel's.
+
+// Lane 0: geometry of row rr into *geo and the bulk copies of its P and dP into `stage`.
+template <typename T>
+__device__ __forceinline__ void rw_issue(const BwdArgs &a, int64_t rr, unsigned char *stage,
+                                         uint64_t *bar, int4 *geo) {
+  constexpr int esz = Io<T>::kEsz;
+  const int4 g = row_geometry(a, rr);
+  *geo = g;
+  const uint32_t bytes = ((uint32_t)g.x * esz + 15u) & ~15u;  // never past the row
+  const uint32_t bar_a = smem_addr(bar);
+  fence_proxy_async_smem();  // the warp's reads of this buffer come before the copies
+  mbar_arrive_expect_tx(bar_a, 2u * bytes);
+  if (bytes) {
+    const size_t off = (size_t)rr * a.ld * esz;
+    bulk_g2s(smem_addr(stage), static_cast<const unsigned char *>(a.probs) + off, bytes, bar_a);
+    bulk_g2s(smem_addr(stage + a.stage_bytes), static_cast<const unsigned char *>(a.dprobs) + off,
+             bytes, bar_a);
+  }
+}
+
+template <typename T>
+__global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  const int nw = blockDim.x >> 5;
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NS = a.stages;  // row buffers per warp
+  const size_t slot = 2 * (size_t)a.stage_bytes;
+  const int T4 = (a.T + 3) & ~3;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem) + w * NS;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes) + w * NS;
+  unsigned char *ring = smem + kBarBytes + kGeoBytes + (size_t)w * NS * slot;
+  float *td = reinterpret_cast<float *>(smem + kBarBytes + kGeoBytes + (size_t)nw * NS * slot) +
+              w * T4;
+
+  const int64_t GW = (int64_t)gridDim.x * nw;     // warps in the grid
+  const int64_t r0 = (int64_t)blockIdx.x * nw + w;  // this warp's first row
+  const int64_t nmine = r0 < a.rows ? (a.rows - 1 - r0) / GW + 1 : 0;
+  const bool stall = a.test_stall && blockIdx.x == 0 && w == 0;
+
+  if (lane == 0) {
+    for (int t = 0; t < NS; ++t) mbar_init(smem_addr(&full[t]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  uint32_t issued = 0, last_ph = 0;
+  if (lane == 0)
+    for (int t = 0; t < NS && t < nmine; ++t)
+      if (!(stall && t == 0)) {  // test only: the very first copies are never issued
+        rw_issue<T>(a, r0 + t * GW, ring + (size_t)t * slot, &full[t], &geos[t]);
+        issued |= 1u << t;
+      }
+
+  int s = 0;
+  uint32_t ph = 0;
+  bool ok = true;
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * GW;
+    unsigned char *sp = ring + (size_t)s * slot;
+    // every lane waits; the warp stops as one if any lane's wait ran out
+    const bool landed = mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
+    if (!__all_sync(kFull, landed)) {
+      if (lane == 0) raise_device_error(a.err, kDevErrTimeout);
+      ok = false;
+      break;
+    }
+    const int4 g = geos[s];
+    const int lim = g.x;
+    const int Te = (lim + kTileK - 1) / kTileK;
+    const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+
+    // ---- pass 1: tile partials of delta, then their sum left to right (every lane)
+    delta_partials<T>(sp, sp + a.stage_bytes, Te, 0, 1, lane, lim, km, td);
+    __syncwarp();
+    float delta = 0.0f;
+    {
+      int t = 0;
+      for (; t + 4 <= Te; t += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(td + t);
+        delta = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(delta, v.x), v.y), v.z), v.w);
+      }
+      for (; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
+    }
+    if (lane == 0 && a.delta) a.delta[r] = delta;
+
+    // ---- pass 2: dScores
+    unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
+    const bool ovec = a.out_vec != 0;
+    grad_tiles<T>(sp, sp + a.stage_bytes, Te, 0, 1, lane, lim, km, delta, grow, 0, a.L, ovec);
+    for (int t = Te; t < a.T; ++t) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+    __syncwarp();  // td is rewritten by the next row; every lane is done with the buffer
+    if (lane == 0 && k + NS < nmine) {
+      rw_issue<T>(a, r + NS * GW, sp, &full[s], &geos[s]);
+      issued |= 1u << s;
+      last_ph = (last_ph & ~(1u << s)) | ((ph ^ 1u) << s);
+    }
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  // every copy this warp issued has landed before it exits
+  if (!ok && lane == 0)
+    for (int t = 0; t < NS; ++t)
+      if (issued & (1u << t))
+        mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+}
+
+const void *bwd_rowwarp_fn(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<float>);
+    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__nv_bfloat16>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__half>);
+  }
+  return nullptr;
+}
+
 // ------------------------------------------------ rows longer than shared memory (streaming)
 //
 // As in the forward: a row too long to stage is read twice, in segments of a.seg_tiles tiles
@@ -556,8 +687,27 @@ cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
   }
+  cudaError_t e = cudaFuncSetAttribute(bwd_rowwarp_fn(dt),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(bwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_smem);
+}
+
+size_t bwd_rowwarp_smem(int warps, int stages, size_t stage_bytes, int T) {
+  return (size_t)kBarBytes + kGeoBytes + (size_t)warps * stages * 2 * stage_bytes +
+         (size_t)warps * ((T + 3) & ~3) * sizeof(float);
+}
+
+cudaError_t bwd_rowwarp_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, bwd_rowwarp_fn(dt), threads,
+                                                       smem);
+}
+
+cudaError_t bwd_rowwarp_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                               cudaStream_t s) {
+  void *args[] = {const_cast<BwdArgs *>(&a)};
+  return cudaLaunchKernel(bwd_rowwarp_fn(dt), dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {

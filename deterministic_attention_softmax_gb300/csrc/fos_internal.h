@@ -90,6 +90,11 @@ cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
+// Short rows, one warp per row (P and dP of a row per buffer; T4 floats of partials per warp).
+size_t bwd_rowwarp_smem(int warps, int stages, size_t stage_bytes, int T);
+cudaError_t bwd_rowwarp_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t bwd_rowwarp_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
+                               cudaStream_t s);
 cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t bwd_stream_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
                               cudaStream_t s);

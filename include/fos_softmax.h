@@ -16,9 +16,9 @@
  * ld-1 are never read or written.  LSE and delta are float32 [rows]; sink and d_sink are
  * float32 [heads].
  *
- * Short rows.  Forward rows of at most 8 tiles (2,048 keys) with 16-byte aligned rows are
- * taken one warp per row (warps_per_cta then counts those warps, stages their row buffers per
- * warp); the arithmetic is the same, so the bits are too.
+ * Short rows.  Rows of at most 8 tiles (2,048 keys) with 16-byte aligned rows are taken one
+ * warp per row, forward and backward (warps_per_cta then counts those warps, stages their row
+ * buffers per warp); the arithmetic is the same, so the bits are too.
  *
  * Long rows.  A row is normally staged whole in shared memory (up to about 57k fp32 / 113k
  * bf16 keys forward, half that backward).  Longer rows are read twice, in segments of 16
@@ -124,9 +124,9 @@ typedef struct fos_launch {
                             anyway by rows too long to stage; same bits) */
   int64_t wait_timeout_ns; /* 0 = default (2 s): limit of every bounded wait in a kernel */
   int32_t test_stall;    /* 0; 1 = CTA 0 waits on a copy that is never issued (test only) */
-  int32_t generic;       /* 0 = auto; 1 = the general one-CTA-per-row kernel only: neither the
-                            instance specialised for unmasked rows nor, forward, the
-                            one-warp-per-row kernel for rows of at most 8 tiles (same bits) */
+  int32_t generic;       /* 0 = auto; 1 = the general one-CTA-per-row kernels only: neither the
+                            instances specialised for unmasked rows nor the one-warp-per-row
+                            kernels for rows of at most 8 tiles (same bits) */
 } fos_launch;
 
 /*

@@ -1,7 +1,8 @@
-"""Rows of at most 8 tiles go to the one-warp-per-row forward kernel by default; ``generic=1``
-keeps them on the CTA kernel.  Both must give the same bits (P and LSE) for every mask, a
-sink, every dtype, and any geometry of the one-warp kernel (warps per CTA, buffers per warp,
-CTAs).  Parity against the oracle for short rows is covered by the small parity grid."""
+"""Rows of at most 8 tiles go to the one-warp-per-row kernels by default (forward and
+backward); ``generic=1`` keeps them on the CTA kernels.  Both must give the same bits (P, LSE,
+dScores, delta) for every mask, a sink, every dtype, and any geometry of the one-warp kernels
+(warps per CTA, buffers per warp, CTAs).  Parity against the oracle for short rows is covered by
+the small parity grid."""
 
 import pytest
 import torch
@@ -21,6 +22,12 @@ def fwd(c, launch=None):
     return fos.fos_softmax_fwd(c["x"], sink=c["sink"], launch=launch, **kw)
 
 
+def bwd(c, p, launch=None):
+    kw = dict(batch=c["B"], heads=c["H"], q_len=c["Sq"], causal=c["causal"],
+              kv_valid_len=c["kv"], key_mask=c["km"])
+    return fos.fos_softmax_bwd(p, c["dp"], launch=launch, **kw)
+
+
 @pytest.mark.parametrize("dtype,L", [(torch.bfloat16, 8), (torch.bfloat16, 200),
                                      (torch.bfloat16, 256), (torch.bfloat16, 264),
                                      (torch.bfloat16, 1000), (torch.bfloat16, 2048),
@@ -31,8 +38,11 @@ def test_one_warp_rows_match_the_cta_kernel(dtype, L, mask):
     c = make_case(dtype, L, mask, B=3, H=4, Sq=37, seed=7)
     p, lse = fwd(c)
     p2, lse2 = fwd(c, CTA)
+    ds, delta = bwd(c, p)
+    ds2, delta2 = bwd(c, p, CTA)
     torch.cuda.synchronize()
     assert bits_equal(p, p2) and bits_equal(lse, lse2)
+    assert bits_equal(ds, ds2) and bits_equal(delta, delta2)
     assert fos.fos_device_error() == 0
 
 
@@ -46,8 +56,11 @@ def test_one_warp_geometry_does_not_change_bits(opts):
     c = make_case(torch.bfloat16, 2048, "all", B=2, H=3, Sq=129, seed=3)
     ref = fwd(c, CTA)
     out = fwd(c, fos.Launch(**opts))
+    gref = bwd(c, ref[0], CTA)
+    gout = bwd(c, ref[0], fos.Launch(**opts))
     torch.cuda.synchronize()
     assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1])
+    assert bits_equal(gref[0], gout[0]) and bits_equal(gref[1], gout[1])
 
 
 def test_unaligned_short_rows_fall_back_to_plain_loads():
@@ -61,3 +74,7 @@ def test_unaligned_short_rows_fall_back_to_plain_loads():
     with pytest.raises(fos.FosError) as e:
         fos.fos_softmax_fwd(x, launch=fos.Launch(load_path=1))
     assert e.value.status == 2
+    dp = torch.randn(40 * 512 + 1, device="cuda").to(torch.bfloat16)[1:].view(40, 512)
+    ds, delta = fos.fos_softmax_bwd(p, dp)  # unaligned dP: the CTA kernel, plain loads
+    ds2, delta2 = fos.fos_softmax_bwd(p, dp.clone())
+    assert bits_equal(ds, ds2) and bits_equal(delta, delta2)
