@@ -268,6 +268,34 @@ constexpr int kRowWarpStages = 2;
 // the causal sink workload).
 constexpr int kRowWarpStagesBwd = 1;
 
+// Row arguments of a one-warp-per-row launch (bulk copies, whole rows per buffer).
+void fill_rowwarp_args(const fos_desc *desc, int esz, int64_t row_base, int64_t nrows, int T,
+                       int stages, size_t stage_bytes, const void *output,
+                       const fos_launch *launch, const DevInfo &dev, RowArgs *a) {
+  a->rows = nrows;
+  a->row_base = row_base;
+  a->ld = desc->ld;
+  a->L = desc->key_len;
+  a->heads = desc->heads;
+  a->q_len = desc->q_len;
+  a->causal = desc->causal;
+  a->kv_valid_len = desc->kv_valid_len;
+  a->key_mask = desc->key_mask;
+  a->T = T;
+  a->stages = stages;
+  a->stage_bytes = (uint32_t)stage_bytes;
+  a->seg_tiles = 0;
+  a->use_bulk = 1;
+  a->in_vec = 1;
+  a->out_vec = (((desc->ld * esz) & 15) == 0 && aligned16(output)) ? 1 : 0;
+  a->timeout_ns = (launch && launch->wait_timeout_ns) ? (uint64_t)launch->wait_timeout_ns
+                                                      : kDefaultTimeoutNs;
+  a->test_stall = launch ? launch->test_stall : 0;
+  a->need_geo = (desc->causal || desc->kv_valid_len || desc->key_mask) ? 1 : 0;
+  a->geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
+  a->err = dev.err;
+}
+
 // The one-warp-per-row forward: needs bulk copies (FOS_ERR_UNSUPPORTED otherwise, so the
 // caller can fall back to the CTA kernel with plain loads).
 fos_status run_fwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
@@ -305,28 +333,8 @@ fos_status run_fwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   if ((int64_t)grid > need) grid = (int)need;
 
   FwdArgs a{};
-  a.rows = nrows;
-  a.row_base = row_base;
-  a.ld = desc->ld;
-  a.L = desc->key_len;
-  a.heads = desc->heads;
-  a.q_len = desc->q_len;
-  a.causal = desc->causal;
-  a.kv_valid_len = desc->kv_valid_len;
-  a.key_mask = desc->key_mask;
-  a.T = T;
-  a.stages = stages;
-  a.stage_bytes = (uint32_t)stage_bytes;
-  a.seg_tiles = 0;
-  a.use_bulk = 1;
-  a.in_vec = 1;
-  a.out_vec = (((desc->ld * esz) & 15) == 0 && aligned16(probs)) ? 1 : 0;
-  a.timeout_ns = (launch && launch->wait_timeout_ns) ? (uint64_t)launch->wait_timeout_ns
-                                                     : kDefaultTimeoutNs;
-  a.test_stall = launch ? launch->test_stall : 0;
-  a.need_geo = (desc->causal || desc->kv_valid_len || desc->key_mask || desc->sink) ? 1 : 0;
-  a.geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
-  a.err = dev.err;
+  fill_rowwarp_args(desc, esz, row_base, nrows, T, stages, stage_bytes, probs, launch, dev, &a);
+  if (desc->sink) a.need_geo = 1;  // the merge needs the row's head
   a.scores = scores;
   a.probs = probs;
   a.lse = lse;
@@ -436,28 +444,7 @@ fos_status run_bwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   if ((int64_t)grid > need) grid = (int)need;
 
   BwdArgs a{};
-  a.rows = nrows;
-  a.row_base = row_base;
-  a.ld = desc->ld;
-  a.L = desc->key_len;
-  a.heads = desc->heads;
-  a.q_len = desc->q_len;
-  a.causal = desc->causal;
-  a.kv_valid_len = desc->kv_valid_len;
-  a.key_mask = desc->key_mask;
-  a.T = T;
-  a.stages = stages;
-  a.stage_bytes = (uint32_t)stage_bytes;
-  a.seg_tiles = 0;
-  a.use_bulk = 1;
-  a.in_vec = 1;
-  a.out_vec = (((desc->ld * esz) & 15) == 0 && aligned16(dscores)) ? 1 : 0;
-  a.timeout_ns = (launch && launch->wait_timeout_ns) ? (uint64_t)launch->wait_timeout_ns
-                                                     : kDefaultTimeoutNs;
-  a.test_stall = launch ? launch->test_stall : 0;
-  a.need_geo = (desc->causal || desc->kv_valid_len || desc->key_mask) ? 1 : 0;
-  a.geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
-  a.err = dev.err;
+  fill_rowwarp_args(desc, esz, row_base, nrows, T, stages, stage_bytes, dscores, launch, dev, &a);
   a.probs = probs;
   a.dprobs = dprobs;
   a.dscores = dscores;
