@@ -3,6 +3,7 @@
 // Host side only: argument validation, the choice of load path and launch geometry, the
 // per-device set-up (SM count, shared-memory limit, kernel attributes, the address of the
 // device error word) and the status strings.  None of these choices changes a result bit.
+#include <cuda_occupancy.h>
 #include <limits.h>
 #include <stdint.h>
 
@@ -30,6 +31,9 @@ struct DevInfo {
   int index = 0;
   int sms = 0;
   int max_smem = 0;  // opt-in dynamic shared memory per block
+  size_t smem_per_sm = 0;
+  size_t reserved_smem = 0;  // shared memory the system keeps per block
+  cudaOccDeviceProp occ;     // for residency counted on the host
   unsigned *err = nullptr;
 };
 
@@ -48,6 +52,11 @@ fos_status device_info(DevInfo **out) {
         cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess)
       return FOS_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FOS_ERR_CUDA;
+    d.occ = cudaOccDeviceProp(prop);
+    d.smem_per_sm = prop.sharedMemPerMultiprocessor;
+    d.reserved_smem = prop.reservedSharedMemPerBlock;
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return FOS_ERR_CUDA;
     d.err = static_cast<unsigned *>(p);
@@ -127,6 +136,48 @@ cudaError_t resident_ctas(int dev_index, uint32_t key, int threads, size_t smem,
   if (memo.size() >= 4096) memo.clear();
   memo[k] = *per_sm;
   return cudaSuccess;
+}
+
+// CTAs per SM of a kernel that allocates `cols` tensor-memory columns per CTA, from its
+// attributes, block size and dynamic shared memory.  The runtime's occupancy query counts such
+// a kernel as filling its SM (the columns are allocated at run time), so the count comes from
+// the occupancy calculator of cuda_occupancy.h at the full shared-memory carveout instead.
+// `fit` is that count; `per_sm` is it capped by the SM's 512 columns.
+cudaError_t tmem_resident_ctas(const DevInfo &d, const cudaFuncAttributes &fa, int threads,
+                               size_t smem, uint32_t cols, int *per_sm, int *fit = nullptr) {
+  cudaOccFuncAttributes oa(fa);
+  cudaOccDeviceState st;
+  st.carveoutConfig = SHAREDMEM_CARVEOUT_MAX_SHARED;
+  cudaOccResult r;
+  if (cudaOccMaxActiveBlocksPerMultiprocessor(&r, &d.occ, &oa, &st, threads, smem) !=
+      CUDA_OCC_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int cap = (int)(kTmemColsPerSm / cols);
+  if (fit) *fit = r.activeBlocksPerMultiprocessor;
+  *per_sm = r.activeBlocksPerMultiprocessor < cap ? r.activeBlocksPerMultiprocessor : cap;
+  return cudaSuccess;
+}
+
+// Dynamic shared memory for a tensor-memory launch: at least `smem`, and enough that no SM
+// takes more CTAs than its columns serve (a CTA past that would wait in its allocation until
+// another CTA of the launch exits).
+cudaError_t tmem_pad_smem(const DevInfo &d, const cudaFuncAttributes &fa, int threads,
+                          uint32_t cols, size_t *smem) {
+  const int cap = (int)(kTmemColsPerSm / cols);
+  for (int iter = 0; iter < 64; ++iter) {
+    int per_sm = 0, fit = 0;
+    cudaError_t e = tmem_resident_ctas(d, fa, threads, *smem, cols, &per_sm, &fit);
+    if (e != cudaSuccess) return e;
+    if (fit <= cap) return cudaSuccess;
+    // the smallest footprint that leaves room for at most `cap` CTAs, then 128-byte steps
+    const size_t want = d.smem_per_sm / (size_t)(cap + 1) + 1;
+    const size_t used = d.reserved_smem + fa.sharedSizeBytes;
+    size_t next = want > used ? want - used : 0;
+    next = (next + 127) & ~(size_t)127;
+    *smem = next > *smem ? next : *smem + 128;
+    if (*smem > (size_t)d.max_smem) return cudaErrorInvalidValue;
+  }
+  return cudaErrorInvalidValue;
 }
 
 // Geometry of a row-kernel launch.
@@ -389,18 +440,30 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask && !desc->sink &&
                     aligned16(scores) && aligned16(probs) && ((desc->ld * esz) & 15) == 0 &&
                     (((int64_t)desc->key_len * esz) & 15) == 0;
+  // Parked e_j take tensor-memory columns; residency is then counted here (see
+  // tmem_resident_ctas) and shared memory padded so that no SM takes more CTAs than it has
+  // columns for.
+  const uint32_t cols = in_regs ? fwd_tmem_cols(warps, kt) : 0u;
+  cudaFuncAttributes fa;
+  if (fwd_attributes(dtype, kt, fast, &fa) != cudaSuccess) return FOS_ERR_CUDA;
   // ring of up to 24 KB per CTA: rows are consumed right after their tile pass
   const uint32_t key = 0x100u | ((uint32_t)dtype << 4) | ((uint32_t)kt << 1) | (fast ? 1u : 0u);
+  const DevInfo &dv = *dev;
   st = plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev, fwd_extra_smem,
-                 warps, 24 * 1024, key, [dtype, kt, fast](int th, size_t sm, int *n) {
+                 warps, 24 * 1024, key | (cols << 8),
+                 [dtype, kt, fast, cols, &fa, &dv](int th, size_t sm, int *n) {
+                   if (cols) return tmem_resident_ctas(dv, fa, th, sm, cols, n);
                    return fwd_occupancy(dtype, kt, fast, th, sm, n);
                  },
                  &a, &pl);
   if (st != FOS_OK) return st;
+  if (cols && tmem_pad_smem(*dev, fa, pl.threads, cols, &pl.smem) != cudaSuccess)
+    return FOS_ERR_UNSUPPORTED;
   a.scores = scores;
   a.probs = probs;
   a.lse = lse;
   a.sink = desc->sink;
+  a.tmem_cols = cols;
   if (desc->sink) a.need_geo = 1;  // the merge needs the row's head
   if (fwd_launch(dtype, kt, fast && a.use_bulk && a.out_vec, a, pl.grid, pl.threads, pl.smem,
                  stream) != cudaSuccess)

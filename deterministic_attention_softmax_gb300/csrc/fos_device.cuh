@@ -346,4 +346,85 @@ __device__ __forceinline__ void raise_device_error(unsigned *err, unsigned code)
   *reinterpret_cast<volatile unsigned *>(err) = code;
 }
 
+// ------------------------------------------------------------------ tensor memory (tcgen05)
+//
+// The forward parks e_j in tensor memory between its two passes instead of holding them in
+// registers, which is what bounds its CTAs per SM otherwise.  An SM has 512 columns of 128
+// lanes x 32 bits; a CTA allocates a power of two of at least 32 columns for its lifetime, and
+// warp w may touch only lanes 32 * (w % 4) .. 32 * (w % 4) + 31.  Values go through unchanged
+// (32-bit moves), so parking changes no result bit.  Address: lane in bits 31..16, column in
+// bits 15..0.
+
+// One warp: allocate `ncols` columns, their base address written to shared memory at `slot`,
+// and give up the right to allocate again (this CTA allocates once).
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// One warp (the allocating one): free the columns.  Every tensor-memory access of the CTA must
+// be complete and ordered before it (tmem_fence_before, a barrier, tmem_fence_after).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Warp-wide: each lane writes its 8 values to 8 consecutive columns of its own lane.
+__device__ __forceinline__ void tmem_st8(uint32_t ta, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(ta),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+
+// Wait until this thread's earlier tmem_st8 have completed (before reading them back).
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Warp-wide: each lane reads 8 (or 16) consecutive columns of its own lane.  The load and its
+// wait are one statement, so the registers are never used before the data has arrived.
+__device__ __forceinline__ void tmem_ld8(uint32_t ta, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(ta)
+      : "memory");
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = __uint_as_float(r[q]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t ta, float (&v)[8], float (&u)[8]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(ta)
+      : "memory");
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    v[q] = __uint_as_float(r[q]);
+    u[q] = __uint_as_float(r[8 + q]);
+  }
+}
+
 }  // namespace fos

@@ -17,10 +17,11 @@
 //            per tile, c_t = exp(m_t - M) / S, and LSE = M + log S.
 //   pass 2   P_j = e_j * c_t, rounded once to the I/O dtype, 16-byte stores.
 //
-// The two tiles of a pair are independent, so their shuffle trees and exponentials overlap;
-// by default a CTA has ceil(T/2) warps so that a row is one pair per warp.  e_j stays in
-// registers when every warp has at most KT tiles (register mode, whose stage is released right
-// after pass 1); longer rows recompute e_j from the staged row in pass 2 (same bits).  Masked
+// The two tiles of a pair are independent, so their shuffle trees and exponentials overlap.
+// When every warp has at most KT tiles, e_j are parked in tensor memory between the passes
+// (each warp in its own lane quarter and columns) and the stage is released right after pass
+// 1; registers then hold one tile pair at a time, which lets twice the CTAs share an SM.
+// Longer rows recompute e_j from the staged row in pass 2 (same bits).  Masked
 // keys (causal bound, valid length, key mask, -inf input) enter as -inf; tiles past the row's
 // last candidate key are neither read nor reduced, and their P is written as +0.
 #include <float.h>
@@ -265,8 +266,7 @@ __device__ void fwd_produce(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmi
 // kFast: the common case fixed at compile time (bulk copies, every row in registers, no mask,
 // no sink, 16-byte aligned output).  Both instances do the same arithmetic in the same order.
 template <typename T, int KT, bool kFast>
-__global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112)))
-    fos_fwd_kernel(const FwdArgs a) {
+__global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -277,6 +277,7 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
   float *tm = reinterpret_cast<float *>(ring + (size_t)a.stages * a.stage_bytes);
   float *ts = tm + T4;
   float *tc = ts + T4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tc + (T4 > 64 ? T4 : 64));
 
   const int tid = threadIdx.x;
   const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
@@ -288,24 +289,35 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
   if (r0 >= a.rows) return;
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
-  const bool reg_mode = kFast || a.T <= nw * KT;  // every row's e_j fit in registers
+  // park mode: every warp has at most KT tiles and the host gave tensor-memory columns for them
+  // (the fast instance is only launched so)
+  const bool park = kFast || a.tmem_cols != 0;
   const bool use_bulk = kFast || a.use_bulk != 0;
 
-  if (use_bulk) {
-    if (tid == 0) {
-      for (int t = 0; t < NS; ++t) {
-        mbar_init(smem_addr(&full[t]), 1);
-        mbar_init(smem_addr(&empty[t]), nw);
-      }
-      fence_mbar_init();
+  if (tid == 0 && use_bulk) {
+    for (int t = 0; t < NS; ++t) {
+      mbar_init(smem_addr(&full[t]), 1);
+      mbar_init(smem_addr(&empty[t]), nw);
     }
-    __syncthreads();
+    fence_mbar_init();
+  }
+  if (park) {
+    if (w == 0) tmem_alloc(smem_addr(tmem_slot), a.tmem_cols);
+    tmem_fence_before();
+  }
+  __syncthreads();
+  uint32_t tbase = 0;
+  if (park) {
+    tmem_fence_after();
+    tbase = *tmem_slot;
   }
   if (w == nw) {
     if (use_bulk && lane == 0)
       fwd_produce<T>(a, r0, G, nmine, full, empty, geos, ring, a.test_stall && blockIdx.x == 0);
     return;
   }
+  // this warp's tile slots: lane quarter w % 4, KT * 8 columns from (w / 4) * KT * 8
+  const uint32_t tw = tbase + ((uint32_t)((w & 3) * 32) << 16) + (uint32_t)((w >> 2) * KT * 8);
 
   // stage index and phase parity of row k, carried rather than computed
   int s = 0;
@@ -332,17 +344,23 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
     const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: tile statistics, two tiles at a time
-    float e[KT][8];
-    if (reg_mode) {
+    if (park) {
 #pragma unroll
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
-        if (t1 < Te)
-          tile_stats2<T>(stage, t0, t1, lane, lim, km, e[kk], e[kk + 1], tm, ts);
-        else if (t0 < Te)
-          tile_stats1<T>(stage, t0, lane, lim, km, e[kk], tm, ts);
+        float e0[8], e1[8];
+        if (t1 < Te) {
+          tile_stats2<T>(stage, t0, t1, lane, lim, km, e0, e1, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+          tmem_st8(tw + kk * 8 + 8, e1);
+        } else if (t0 < Te) {
+          tile_stats1<T>(stage, t0, lane, lim, km, e0, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+        }
       }
-      if (use_bulk) {  // the stage is free: e_j are in registers
+      if (use_bulk) {  // the stage is free: e_j are parked
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
       }
@@ -359,9 +377,10 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
     }
 
     if (compute_sync_or(ncomp, timed_out)) {
-      // A copy never landed: record it and stop (the producer drains the copies in flight).
+      // A copy never landed: record it and stop (the producer drains the copies in flight;
+      // the tensor memory is freed below).
       if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
-      return;
+      break;
     }
 
     // ---- merge (warp 0)
@@ -379,16 +398,21 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
     // ---- pass 2: P = e * c_t, one rounding, 16-byte stores
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
     const bool ovec = kFast || a.out_vec != 0;
-    if (reg_mode) {
+    if (park) {
+      __syncwarp();
+      tmem_wait_st();  // this warp's pass-1 values have landed
 #pragma unroll
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
+        float e0[8], e1[8];
         if (t1 < Te) {
+          tmem_ld16(tw + kk * 8, e0, e1);
           const float c0 = tc[t0], c1 = tc[t1];
-          tile_store<T>(prow, t0, lane, a.L, ovec, e[kk], c0);
-          tile_store<T>(prow, t1, lane, a.L, ovec, e[kk + 1], c1);
+          tile_store<T>(prow, t0, lane, a.L, ovec, e0, c0);
+          tile_store<T>(prow, t1, lane, a.L, ovec, e1, c1);
         } else if (t0 < Te) {
-          tile_store<T>(prow, t0, lane, a.L, ovec, e[kk], tc[t0]);
+          tmem_ld8(tw + kk * 8, e0);
+          tile_store<T>(prow, t0, lane, a.L, ovec, e0, tc[t0]);
         }
       }
     } else {
@@ -410,6 +434,15 @@ __global__ void __maxnreg__(KT <= 2 ? 64 : (KT <= 4 ? 80 : (KT <= 6 ? 96 : 112))
     }
     // Tile t's tm entry is written (pass 1) and re-read (pass 2) by warp t % nw only, and tc
     // is rewritten after the next row's first barrier: no barrier is needed here.
+  }
+  if (park) {  // every compute warp is done with its columns: free them
+    tmem_wait_st();
+    tmem_fence_before();
+    compute_sync(ncomp);
+    if (w == 0) {
+      tmem_fence_after();
+      tmem_dealloc(tbase, a.tmem_cols);
+    }
   }
 }
 
@@ -801,7 +834,17 @@ size_t fwd_extra_smem(int T, int stages) {
   (void)stages;
   // tm and ts (T rounded up to 4), then tc, which is also the merge's 64-float scratch
   const int T4 = (T + 3) & ~3;
-  return (size_t)kBarBytes + kGeoBytes + (size_t)(2 * T4 + (T4 > 64 ? T4 : 64)) * sizeof(float);
+  // (and 16 bytes for the tensor-memory address)
+  return (size_t)kBarBytes + kGeoBytes + (size_t)(2 * T4 + (T4 > 64 ? T4 : 64)) * sizeof(float) +
+         16;
+}
+
+uint32_t fwd_tmem_cols(int warps, int kt) {
+  // warps sharing a lane quarter take consecutive column ranges of kt * 8
+  const uint32_t need = (uint32_t)(((warps + 3) / 4) * kt * 8);
+  uint32_t cols = 32;
+  while (cols < need) cols <<= 1;
+  return cols;
 }
 
 int fwd_tiles_per_warp(int T, int warps) {
@@ -833,6 +876,11 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
     for (bool fast : {false, true}) {
       cudaError_t e = cudaFuncSetAttribute(fwd_fn(dt, kt, fast),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+      // all of the SM's on-chip memory as shared memory: the host's residency count for these
+      // instances (which allocate tensor memory) assumes it
+      e = cudaFuncSetAttribute(fwd_fn(dt, kt, fast), cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
     }
   for (int kt : {2, 4, 8}) {
@@ -870,6 +918,10 @@ cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int thre
                               cudaStream_t s) {
   void *args[] = {const_cast<FwdArgs *>(&a)};
   return cudaLaunchKernel(fwd_stream_fn(dt), dim3(grid), dim3(threads), args, smem, s);
+}
+
+cudaError_t fwd_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa) {
+  return cudaFuncGetAttributes(fa, fwd_fn(dt, kt, fast));
 }
 
 cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,

@@ -40,8 +40,15 @@ struct FwdArgs : RowArgs {
   const void *scores;
   void *probs;
   float *lse;
-  const float *sink;  // [heads] or null
+  const float *sink;   // [heads] or null
+  uint32_t tmem_cols;  // tensor-memory columns a CTA allocates to park e_j; 0: none (e_j are
+                       // recomputed in the second pass)
 };
+
+// Tensor-memory columns per SM, and the columns a forward CTA of `warps` compute warps with
+// `kt` tiles per warp allocates (a power of two, at least 32).
+constexpr uint32_t kTmemColsPerSm = 512;
+uint32_t fwd_tmem_cols(int warps, int kt);
 
 struct BwdArgs : RowArgs {
   const void *probs;
@@ -63,8 +70,9 @@ size_t fwd_extra_smem(int T, int stages);
 size_t bwd_extra_smem(int T, int stages);
 
 // Kernel instances per dtype: set the dynamic shared-memory limit, query residency, launch.
-// The forward keeps e_j of `kt` tiles per warp in registers (kt = 2, 4, 6 or 8); `fast`
-// selects the instance specialised for the common case (same arithmetic).
+// The forward parks e_j of `kt` tiles per warp (kt = 2, 4, 6 or 8) in tensor memory between
+// its passes when a.tmem_cols is set; `fast` selects the instance specialised for the common
+// case (same arithmetic).
 int fwd_tiles_per_warp(int T, int warps);
 // Default compute warps per CTA (1..16).
 int fwd_default_warps(int T);
@@ -72,6 +80,10 @@ int bwd_default_warps(int T);
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,
                           int *blocks_per_sm);
+// Registers, static shared memory and limits of a forward CTA instance (for residency
+// computed on the host: the runtime's query counts a kernel that allocates tensor memory as
+// filling its SM).
+cudaError_t fwd_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa);
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
 // Rows of at most 8 tiles, one warp per row: kt = 2, 4 or 8 tiles kept in registers; `warps`

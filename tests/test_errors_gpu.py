@@ -20,14 +20,21 @@ def inputs(dtype=torch.bfloat16, rows=600, L=2048):
     return x, dp
 
 
+# staged rows (one warp per row at 2048 keys), streamed segments, the CTA kernels that park
+# e_j in tensor memory (generic at 2048 keys, specialised at 4352)
+PATHS = {"staged": (2048, dict(load_path=1)), "streamed": (2048, dict(load_path=3)),
+         "cta": (2048, dict(load_path=1, generic=1)), "cta_fast": (4352, dict(load_path=1))}
+
+
 @pytest.mark.parametrize("which", ["fwd", "bwd"])
-@pytest.mark.parametrize("path", [1, 3])  # staged rows, streamed segments
+@pytest.mark.parametrize("path", list(PATHS))
 def test_stalled_copy_times_out_and_context_survives(which, path):
-    x, dp = inputs()
+    L, opts = PATHS[path]
+    x, dp = inputs(L=L)
     ref_p, ref_lse = fos.fos_softmax_fwd(x)
     ref_ds, ref_delta = fos.fos_softmax_bwd(ref_p, dp)
     assert fos.fos_device_error() == 0
-    stall = fos.Launch(test_stall=1, wait_timeout_ns=20_000_000, load_path=path)
+    stall = fos.Launch(test_stall=1, wait_timeout_ns=20_000_000, **opts)
     if which == "fwd":
         fos.fos_softmax_fwd(x, launch=stall)
     else:

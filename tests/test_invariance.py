@@ -222,3 +222,30 @@ def test_sink_grad_geometry_invariant():
     for warps in (1, 2, 3, 8, 16):
         out = fos.fos_sink_grad(lse, delta, sink, launch=fos.Launch(warps_per_cta=warps), **geo)
         assert bits_equal(ref, out)
+
+
+@pytest.mark.parametrize("warps", list(range(1, 17)))
+def test_every_warp_count_gives_the_same_bits(warps):
+    # The CTA forward parks e_j in tensor memory: warp w in lane quarter w % 4, warps that share
+    # a quarter side by side in its columns.  Every split of a 17-tile row over 1..16 warps
+    # (parked or, past 8 tiles per warp, recomputed) gives the default launch's bits.
+    x = W.normal((600, 4352), 4.0, 43, torch.bfloat16, dev())
+    ref = fos.fos_softmax_fwd(x)
+    out = fos.fos_softmax_fwd(x, launch=fos.Launch(warps_per_cta=warps))
+    torch.cuda.synchronize()
+    assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1])
+    assert fos.fos_device_error() == 0
+
+
+@pytest.mark.parametrize("L,opts", [(4352, dict()), (4352, dict(generic=1)),
+                                    (200, dict(generic=1)), (2048, dict(generic=1, warps_per_cta=1))])
+def test_more_ctas_than_tensor_memory_serves(L, opts):
+    # One CTA per row: at most 512 / (columns per CTA) CTAs can hold tensor memory on an SM at
+    # once.  The launch pads shared memory so that no more are resident; the others start as
+    # resident ones exit.  Same bits as the default grid.
+    x = W.normal((4096, L), 4.0, 44, torch.bfloat16, dev())
+    ref = fos.fos_softmax_fwd(x, launch=fos.Launch(**opts) if opts else None)
+    out = fos.fos_softmax_fwd(x, launch=fos.Launch(ctas=4096, **opts))
+    torch.cuda.synchronize()
+    assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1])
+    assert fos.fos_device_error() == 0
