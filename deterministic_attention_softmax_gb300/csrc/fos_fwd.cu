@@ -317,6 +317,10 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
     return;
   }
   // this warp's tile slots: lane quarter w % 4, KT * 8 columns from (w / 4) * KT * 8
+  // The pair loops stay rolled up to three pairs (their slots are addressed at run time): the
+  // smaller code measured 9-12 % faster on 17- and 18-tile rows, the unrolled one 1-4 % faster
+  // at four pairs.
+  constexpr int kPairUnroll = KT <= 6 ? 1 : KT / 2;
   const uint32_t tw = tbase + ((uint32_t)((w & 3) * 32) << 16) + (uint32_t)((w >> 2) * KT * 8);
 
   // stage index and phase parity of row k, carried rather than computed
@@ -345,7 +349,7 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
 
     // ---- pass 1: tile statistics, two tiles at a time
     if (park) {
-#pragma unroll
+#pragma unroll(kPairUnroll)
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
         float e0[8], e1[8];
@@ -401,7 +405,7 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
     if (park) {
       __syncwarp();
       tmem_wait_st();  // this warp's pass-1 values have landed
-#pragma unroll
+#pragma unroll(kPairUnroll)
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
         float e0[8], e1[8];
@@ -659,7 +663,8 @@ const void *fwd_stream_fn(fos_dtype dt) {
 //
 // A row of at most KT (<= 8) tiles is taken by one warp alone: it waits for the row's copy,
 // runs pass 1 on all its tiles (pairs of neighbouring tiles), folds the tile states with the
-// same merge, and writes P from the e_j it kept in registers.  No barrier joins the warps of a
+// same merge, and writes P from the e_j it parked in tensor memory (its lane quarter w % 4,
+// warps sharing a quarter side by side in its columns).  No barrier joins the warps of a
 // CTA, so the merge of one row does not idle the others.  Each warp keeps its own ring of
 // a.stages row buffers and its lane 0 issues its own copies: the copy of row k + stages goes into
 // the buffer of row k as soon as pass 1 of row k has read it.  The per-tile arithmetic, the
@@ -683,8 +688,7 @@ __device__ __forceinline__ void rw_issue(const FwdArgs &a, int64_t rr, unsigned 
 }
 
 template <typename T, int KT>
-__global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp_kernel(
-    const FwdArgs a) {
+__global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
   constexpr int kStat = 80;  // floats per warp: tm[8], ts[8], tc[64] (tc is the merge scratch)
@@ -695,10 +699,12 @@ __global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp
   uint64_t *full = reinterpret_cast<uint64_t *>(smem) + w * NS;
   int4 *geos = reinterpret_cast<int4 *>(smem + kBarBytes) + w * NS;
   unsigned char *ring = smem + kBarBytes + kGeoBytes + (size_t)w * NS * a.stage_bytes;
-  float *tm = reinterpret_cast<float *>(smem + kBarBytes + kGeoBytes +
-                                        (size_t)nw * NS * a.stage_bytes) + w * kStat;
+  float *stats = reinterpret_cast<float *>(smem + kBarBytes + kGeoBytes +
+                                           (size_t)nw * NS * a.stage_bytes);
+  float *tm = stats + w * kStat;
   float *ts = tm + 8;
   float *tc = tm + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stats + nw * kStat);
 
   const int64_t GW = (int64_t)gridDim.x * nw;           // warps in the grid
   const int64_t r0 = (int64_t)blockIdx.x * nw + w;        // this warp's first row
@@ -709,7 +715,15 @@ __global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp
     for (int t = 0; t < NS; ++t) mbar_init(smem_addr(&full[t]), 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  if (w == 0) tmem_alloc(smem_addr(tmem_slot), a.tmem_cols);
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tw =
+      *tmem_slot + ((uint32_t)((w & 3) * 32) << 16) + (uint32_t)((w >> 2) * KT * 8);
+  // the four-pair loops stay rolled (measured 11 % faster on 8-tile rows), shorter ones are
+  // unrolled (2 % faster on 4-tile rows)
+  constexpr int kPairUnroll = KT >= 8 ? 1 : KT / 2;
   // prologue: the first rows' copies (test only: the very first one is never issued)
   uint32_t issued = 0, last_ph = 0;
   if (lane == 0)
@@ -738,13 +752,19 @@ __global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp
     const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: every tile of the row, two neighbouring tiles at a time
-    float e[KT][8];
-#pragma unroll
+#pragma unroll(kPairUnroll)
     for (int kk = 0; kk < KT; kk += 2) {
-      if (kk + 1 < Te)
-        tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e[kk], e[kk + 1], tm, ts);
-      else if (kk < Te)
-        tile_stats1<T>(stage, kk, lane, lim, km, e[kk], tm, ts);
+      float e0[8], e1[8];
+      if (kk + 1 < Te) {
+        tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e0, e1, tm, ts);
+        __syncwarp();
+        tmem_st8(tw + kk * 8, e0);
+        tmem_st8(tw + kk * 8 + 8, e1);
+      } else if (kk < Te) {
+        tile_stats1<T>(stage, kk, lane, lim, km, e0, tm, ts);
+        __syncwarp();
+        tmem_st8(tw + kk * 8, e0);
+      }
     }
     __syncwarp();  // tm / ts (lane 0) for the merge; every lane is done with the buffer
     if (lane == 0 && k + NS < nmine) {
@@ -763,12 +783,23 @@ __global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp
     __syncwarp();  // tc
     if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
-    // ---- pass 2: P from the e_j kept in registers
+    // ---- pass 2: P from the parked e_j
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
     const bool ovec = a.out_vec != 0;
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk)
-      if (kk < Te) tile_store<T>(prow, kk, lane, a.L, ovec, e[kk], tc[kk]);
+    __syncwarp();
+    tmem_wait_st();
+#pragma unroll(kPairUnroll)
+    for (int kk = 0; kk < KT; kk += 2) {
+      float e0[8], e1[8];
+      if (kk + 1 < Te) {
+        tmem_ld16(tw + kk * 8, e0, e1);
+        tile_store<T>(prow, kk, lane, a.L, ovec, e0, tc[kk]);
+        tile_store<T>(prow, kk + 1, lane, a.L, ovec, e1, tc[kk + 1]);
+      } else if (kk < Te) {
+        tmem_ld8(tw + kk * 8, e0);
+        tile_store<T>(prow, kk, lane, a.L, ovec, e0, tc[kk]);
+      }
+    }
     for (int t = Te; t < a.T; ++t) {
       float z[8];
 #pragma unroll
@@ -787,6 +818,15 @@ __global__ void __maxnreg__(KT <= 2 ? 72 : (KT <= 4 ? 88 : 120)) fos_fwd_rowwarp
     for (int t = 0; t < NS; ++t)
       if (issued & (1u << t))
         mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
+  // every warp is done with its columns: free them
+  __syncwarp();
+  tmem_wait_st();
+  tmem_fence_before();
+  __syncthreads();
+  if (w == 0) {
+    tmem_fence_after();
+    tmem_dealloc(*tmem_slot, a.tmem_cols);
+  }
 }
 
 template <int KT>
@@ -858,17 +898,13 @@ int fwd_tiles_per_warp(int T, int warps) {
 
 int fwd_default_warps(int T) {
   // Fitted to timings of the unmasked and causal bf16 forward on GB300 over 256..16384 keys
-  // (any choice gives the same bits).  The CTA count per SM is set by the registers that hold
-  // e_j, so the aim is few idle tile slots with two to six tiles per warp.
+  // (any choice gives the same bits), with e_j parked in tensor memory: four tiles per warp on
+  // short rows, six on 17..24 tiles, eight (the most a warp parks) on longer ones.
   if (T <= 1) return 1;
-  if (T <= 4) return 2;
-  if (T <= 6) return 3;
-  if (T <= 8) return 2;
-  if (T <= 16) return (T + 3) / 4;  // four tiles per warp
-  if (T <= 24) return (T + 5) / 6;  // six
-  if (T <= 32) return (T + 3) / 4;  // four
-  if (T <= 48) return 8;            // six
-  return 6;                         // e_j recomputed in the second pass
+  if (T <= 16) return (T + 3) / 4;
+  if (T <= 24) return (T + 5) / 6;
+  if (T <= 128) return (T + 7) / 8;  // up to 16 warps
+  return 8;                          // e_j recomputed in the second pass
 }
 
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
@@ -887,15 +923,12 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
     cudaError_t e = cudaFuncSetAttribute(fwd_rowwarp_fn(dt, kt),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fwd_rowwarp_fn(dt, kt), cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
   }
   return cudaFuncSetAttribute(fwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_smem);
-}
-
-cudaError_t fwd_rowwarp_occupancy(fos_dtype dt, int kt, int threads, size_t smem,
-                                  int *blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_rowwarp_fn(dt, kt),
-                                                       threads, smem);
 }
 
 cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
@@ -905,8 +938,13 @@ cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid,
 }
 
 size_t fwd_rowwarp_smem(int warps, int stages, size_t stage_bytes) {
+  // per warp: its buffers and 80 floats of tile statistics; then the tensor-memory address
   return (size_t)kBarBytes + kGeoBytes + (size_t)warps * stages * stage_bytes +
-         (size_t)warps * 80 * sizeof(float);
+         (size_t)warps * 80 * sizeof(float) + 16;
+}
+
+cudaError_t fwd_rowwarp_attributes(fos_dtype dt, int kt, cudaFuncAttributes *fa) {
+  return cudaFuncGetAttributes(fa, fwd_rowwarp_fn(dt, kt));
 }
 
 cudaError_t fwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
@@ -922,12 +960,6 @@ cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int thre
 
 cudaError_t fwd_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa) {
   return cudaFuncGetAttributes(fa, fwd_fn(dt, kt, fast));
-}
-
-cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,
-                          int *blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fwd_fn(dt, kt, fast),
-                                                       threads, smem);
 }
 
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,

@@ -78,19 +78,17 @@ int fwd_tiles_per_warp(int T, int warps);
 int fwd_default_warps(int T);
 int bwd_default_warps(int T);
 cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
-cudaError_t fwd_occupancy(fos_dtype dt, int kt, bool fast, int threads, size_t smem,
-                          int *blocks_per_sm);
-// Registers, static shared memory and limits of a forward CTA instance (for residency
+// Registers, static shared memory and limits of a forward CTA instance (its residency is
 // computed on the host: the runtime's query counts a kernel that allocates tensor memory as
 // filling its SM).
 cudaError_t fwd_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa);
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
-// Rows of at most 8 tiles, one warp per row: kt = 2, 4 or 8 tiles kept in registers; `warps`
-// warps per CTA, each with a.stages row buffers of a.stage_bytes.
+// Rows of at most 8 tiles, one warp per row: kt = 2, 4 or 8 tiles parked in a.tmem_cols
+// tensor-memory columns; `warps` warps per CTA, each with a.stages row buffers of
+// a.stage_bytes.
 size_t fwd_rowwarp_smem(int warps, int stages, size_t stage_bytes);
-cudaError_t fwd_rowwarp_occupancy(fos_dtype dt, int kt, int threads, size_t smem,
-                                  int *blocks_per_sm);
+cudaError_t fwd_rowwarp_attributes(fos_dtype dt, int kt, cudaFuncAttributes *fa);
 cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,
                                size_t smem, cudaStream_t s);
 // Rows longer than shared memory: segments of a.seg_tiles tiles, each read twice.
