@@ -372,10 +372,11 @@ fos_status run_fwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   const int threads = warps * 32;
   // e_j are parked in tensor memory: residency counted here, shared memory padded so that no
   // SM takes more CTAs than it has columns for (see tmem_resident_ctas)
-  const uint32_t cols = fwd_tmem_cols(warps, kt);
+  const uint32_t cols = kt > 2 ? fwd_tmem_cols(warps, kt) : 0u;  // kt 2: registers
   cudaFuncAttributes fa;
   if (fwd_rowwarp_attributes(dtype, kt, &fa) != cudaSuccess) return FOS_ERR_CUDA;
-  if (tmem_pad_smem(dev, fa, threads, cols, &smem) != cudaSuccess) return FOS_ERR_UNSUPPORTED;
+  if (cols && tmem_pad_smem(dev, fa, threads, cols, &smem) != cudaSuccess)
+    return FOS_ERR_UNSUPPORTED;
   int grid = 0;
   if (launch && launch->ctas) {
     grid = launch->ctas;
@@ -401,6 +402,7 @@ fos_status run_fwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   a.probs = probs;
   a.lse = lse;
   a.sink = desc->sink;
+  a.keep_e = 1;
   a.tmem_cols = cols;
   if (fwd_rowwarp_launch(dtype, kt, a, grid, threads, smem, stream) != cudaSuccess)
     return FOS_ERR_CUDA;
@@ -465,7 +467,7 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   // Parked e_j take tensor-memory columns; residency is then counted here (see
   // tmem_resident_ctas) and shared memory padded so that no SM takes more CTAs than it has
   // columns for.
-  const uint32_t cols = in_regs ? fwd_tmem_cols(warps, kt) : 0u;
+  const uint32_t cols = (in_regs && kt > 2) ? fwd_tmem_cols(warps, kt) : 0u;
   cudaFuncAttributes fa;
   if (fwd_attributes(dtype, kt, fast, &fa) != cudaSuccess) return FOS_ERR_CUDA;
   // ring of up to 24 KB per CTA: rows are consumed right after their tile pass
@@ -480,6 +482,7 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   if (st != FOS_OK) return st;
   if (cols && tmem_pad_smem(*dev, fa, pl.threads, cols, &pl.smem) != cudaSuccess)
     return FOS_ERR_UNSUPPORTED;
+  a.keep_e = in_regs ? 1 : 0;
   a.scores = scores;
   a.probs = probs;
   a.lse = lse;

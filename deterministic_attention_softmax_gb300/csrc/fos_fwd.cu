@@ -20,8 +20,9 @@
 // The two tiles of a pair are independent, so their shuffle trees and exponentials overlap.
 // When every warp has at most KT tiles, e_j are parked in tensor memory between the passes
 // (each warp in its own lane quarter and columns) and the stage is released right after pass
-// 1; registers then hold one tile pair at a time, which lets twice the CTAs share an SM.
-// Longer rows recompute e_j from the staged row in pass 2 (same bits).  Masked
+// 1; registers then hold one tile pair at a time, which lets twice the CTAs share an SM.  A
+// single pair per warp (KT = 2) simply stays in registers.  Longer rows recompute e_j from the
+// staged row in pass 2 (same bits).  Masked
 // keys (causal bound, valid length, key mask, -inf input) enter as -inf; tiles past the row's
 // last candidate key are neither read nor reduced, and their P is written as +0.
 #include <float.h>
@@ -266,7 +267,7 @@ __device__ void fwd_produce(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmi
 // kFast: the common case fixed at compile time (bulk copies, every row in registers, no mask,
 // no sink, 16-byte aligned output).  Both instances do the same arithmetic in the same order.
 template <typename T, int KT, bool kFast>
-__global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
+__global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -289,9 +290,11 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
   if (r0 >= a.rows) return;
   const int64_t nmine = (a.rows - 1 - r0) / G + 1;
   const int NS = a.stages;
-  // park mode: every warp has at most KT tiles and the host gave tensor-memory columns for them
-  // (the fast instance is only launched so)
-  const bool park = kFast || a.tmem_cols != 0;
+  // keep mode: every warp has at most KT tiles (the fast instance is only launched so); they
+  // are parked in tensor memory unless one pair per warp stays in registers
+  constexpr bool kRegs = KT == 2;
+  const bool keep = kFast || a.keep_e != 0;
+  const bool park = keep && !kRegs;
   const bool use_bulk = kFast || a.use_bulk != 0;
 
   if (tid == 0 && use_bulk) {
@@ -348,20 +351,34 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
     const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: tile statistics, two tiles at a time
-    if (park) {
+    float er0[8], er1[8];  // kRegs: the warp's pair, kept for pass 2
+    if (keep) {
 #pragma unroll(kPairUnroll)
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
         float e0[8], e1[8];
         if (t1 < Te) {
           tile_stats2<T>(stage, t0, t1, lane, lim, km, e0, e1, tm, ts);
-          __syncwarp();
-          tmem_st8(tw + kk * 8, e0);
-          tmem_st8(tw + kk * 8 + 8, e1);
+          if constexpr (kRegs) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              er0[q] = e0[q];
+              er1[q] = e1[q];
+            }
+          } else {
+            __syncwarp();
+            tmem_st8(tw + kk * 8, e0);
+            tmem_st8(tw + kk * 8 + 8, e1);
+          }
         } else if (t0 < Te) {
           tile_stats1<T>(stage, t0, lane, lim, km, e0, tm, ts);
-          __syncwarp();
-          tmem_st8(tw + kk * 8, e0);
+          if constexpr (kRegs) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) er0[q] = e0[q];
+          } else {
+            __syncwarp();
+            tmem_st8(tw + kk * 8, e0);
+          }
         }
       }
       if (use_bulk) {  // the stage is free: e_j are parked
@@ -402,20 +419,35 @@ __global__ void __maxnreg__(64) fos_fwd_kernel(const FwdArgs a) {
     // ---- pass 2: P = e * c_t, one rounding, 16-byte stores
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
     const bool ovec = kFast || a.out_vec != 0;
-    if (park) {
-      __syncwarp();
-      tmem_wait_st();  // this warp's pass-1 values have landed
+    if (keep) {
+      if (park) {
+        __syncwarp();
+        tmem_wait_st();  // this warp's pass-1 values have landed
+      }
 #pragma unroll(kPairUnroll)
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
         float e0[8], e1[8];
         if (t1 < Te) {
-          tmem_ld16(tw + kk * 8, e0, e1);
+          if constexpr (kRegs) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              e0[q] = er0[q];
+              e1[q] = er1[q];
+            }
+          } else {
+            tmem_ld16(tw + kk * 8, e0, e1);
+          }
           const float c0 = tc[t0], c1 = tc[t1];
           tile_store<T>(prow, t0, lane, a.L, ovec, e0, c0);
           tile_store<T>(prow, t1, lane, a.L, ovec, e1, c1);
         } else if (t0 < Te) {
-          tmem_ld8(tw + kk * 8, e0);
+          if constexpr (kRegs) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) e0[q] = er0[q];
+          } else {
+            tmem_ld8(tw + kk * 8, e0);
+          }
           tile_store<T>(prow, t0, lane, a.L, ovec, e0, tc[t0]);
         }
       }
@@ -688,7 +720,7 @@ __device__ __forceinline__ void rw_issue(const FwdArgs &a, int64_t rr, unsigned 
 }
 
 template <typename T, int KT>
-__global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
+__global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
   constexpr int kStat = 80;  // floats per warp: tm[8], ts[8], tc[64] (tc is the merge scratch)
@@ -715,12 +747,17 @@ __global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
     for (int t = 0; t < NS; ++t) mbar_init(smem_addr(&full[t]), 1);
     fence_mbar_init();
   }
-  if (w == 0) tmem_alloc(smem_addr(tmem_slot), a.tmem_cols);
-  tmem_fence_before();
-  __syncthreads();
-  tmem_fence_after();
+  // one pair per row (KT = 2) stays in registers; longer rows are parked in tensor memory
+  constexpr bool kRegs = KT == 2;
+  if constexpr (!kRegs) {
+    if (w == 0) tmem_alloc(smem_addr(tmem_slot), a.tmem_cols);
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+  }
+  __syncwarp();  // this warp's barriers are initialised
   const uint32_t tw =
-      *tmem_slot + ((uint32_t)((w & 3) * 32) << 16) + (uint32_t)((w >> 2) * KT * 8);
+      kRegs ? 0u : *tmem_slot + ((uint32_t)((w & 3) * 32) << 16) + (uint32_t)((w >> 2) * KT * 8);
   // the four-pair loops stay rolled (measured 11 % faster on 8-tile rows), shorter ones are
   // unrolled (2 % faster on 4-tile rows)
   constexpr int kPairUnroll = KT >= 8 ? 1 : KT / 2;
@@ -752,18 +789,26 @@ __global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
     const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
 
     // ---- pass 1: every tile of the row, two neighbouring tiles at a time
+    float er0[8], er1[8];  // kRegs: the row's pair, kept for pass 2
 #pragma unroll(kPairUnroll)
     for (int kk = 0; kk < KT; kk += 2) {
-      float e0[8], e1[8];
-      if (kk + 1 < Te) {
-        tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e0, e1, tm, ts);
-        __syncwarp();
-        tmem_st8(tw + kk * 8, e0);
-        tmem_st8(tw + kk * 8 + 8, e1);
-      } else if (kk < Te) {
-        tile_stats1<T>(stage, kk, lane, lim, km, e0, tm, ts);
-        __syncwarp();
-        tmem_st8(tw + kk * 8, e0);
+      if constexpr (kRegs) {
+        if (kk + 1 < Te)
+          tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, er0, er1, tm, ts);
+        else if (kk < Te)
+          tile_stats1<T>(stage, kk, lane, lim, km, er0, tm, ts);
+      } else {
+        float e0[8], e1[8];
+        if (kk + 1 < Te) {
+          tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e0, e1, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+          tmem_st8(tw + kk * 8 + 8, e1);
+        } else if (kk < Te) {
+          tile_stats1<T>(stage, kk, lane, lim, km, e0, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+        }
       }
     }
     __syncwarp();  // tm / ts (lane 0) for the merge; every lane is done with the buffer
@@ -783,13 +828,22 @@ __global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
     __syncwarp();  // tc
     if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
-    // ---- pass 2: P from the parked e_j
+    // ---- pass 2: P from the kept e_j
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
     const bool ovec = a.out_vec != 0;
-    __syncwarp();
-    tmem_wait_st();
+    if constexpr (kRegs) {
+      if (1 < Te) {
+        tile_store<T>(prow, 0, lane, a.L, ovec, er0, tc[0]);
+        tile_store<T>(prow, 1, lane, a.L, ovec, er1, tc[1]);
+      } else if (0 < Te) {
+        tile_store<T>(prow, 0, lane, a.L, ovec, er0, tc[0]);
+      }
+    } else {
+      __syncwarp();
+      tmem_wait_st();
+    }
 #pragma unroll(kPairUnroll)
-    for (int kk = 0; kk < KT; kk += 2) {
+    for (int kk = 0; kk < (kRegs ? 0 : KT); kk += 2) {
       float e0[8], e1[8];
       if (kk + 1 < Te) {
         tmem_ld16(tw + kk * 8, e0, e1);
@@ -819,13 +873,15 @@ __global__ void __maxnreg__(64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
       if (issued & (1u << t))
         mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
   // every warp is done with its columns: free them
-  __syncwarp();
-  tmem_wait_st();
-  tmem_fence_before();
-  __syncthreads();
-  if (w == 0) {
-    tmem_fence_after();
-    tmem_dealloc(*tmem_slot, a.tmem_cols);
+  if constexpr (!kRegs) {
+    __syncwarp();
+    tmem_wait_st();
+    tmem_fence_before();
+    __syncthreads();
+    if (w == 0) {
+      tmem_fence_after();
+      tmem_dealloc(*tmem_slot, a.tmem_cols);
+    }
   }
 }
 

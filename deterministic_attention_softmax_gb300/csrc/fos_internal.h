@@ -41,8 +41,10 @@ struct FwdArgs : RowArgs {
   void *probs;
   float *lse;
   const float *sink;   // [heads] or null
-  uint32_t tmem_cols;  // tensor-memory columns a CTA allocates to park e_j; 0: none (e_j are
-                       // recomputed in the second pass)
+  int32_t keep_e;      // CTA kernel: e_j are kept between the passes (every warp has at most
+                       // KT tiles); otherwise they are recomputed in the second pass
+  uint32_t tmem_cols;  // tensor-memory columns a CTA allocates to keep them in; 0 when none
+                       // (two tiles per warp stay in registers)
 };
 
 // Tensor-memory columns per SM, and the columns a forward CTA of `warps` compute warps with
