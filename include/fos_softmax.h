@@ -139,6 +139,10 @@ typedef struct fos_launch {
  *   scores  device [rows, ld] of dtype        (input)
  *   probs   device [rows, ld] of dtype        (output P; may equal scores)
  *   lse     device float [rows]               (output; -inf for a row with nothing valid)
+ * Resources: besides shared memory, each CTA of the forward allocates tensor memory (tcgen05,
+ * at most 256 of an SM's 512 columns) for its lifetime, and it frees it before exiting, on
+ * error paths too.  A kernel of another stream that holds the SM's remaining columns makes the
+ * forward's CTAs wait in their allocation until those are released.
  */
 fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
                            void *probs, float *lse, cudaStream_t stream,
