@@ -264,7 +264,7 @@ __device__ void fwd_produce(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmi
       mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
 }
 
-// kFast: the common case fixed at compile time (bulk copies, every row in registers, no mask,
+// kFast: the common case fixed at compile time (bulk copies, every row's e_j kept, no mask,
 // no sink, 16-byte aligned output).  Both instances do the same arithmetic in the same order.
 template <typename T, int KT, bool kFast>
 __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_kernel(const FwdArgs a) {
