@@ -281,6 +281,8 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t 
   ra->test_stall = l ? l->test_stall : 0;
   ra->need_geo = (d->causal || d->kv_valid_len || d->key_mask) ? 1 : 0;
   ra->geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
+  ra->qdiv = make_fastdiv((uint32_t)d->q_len);
+  ra->hdiv = make_fastdiv((uint32_t)d->heads);
   ra->err = dev.err;
 
   pl->threads = threads;
@@ -348,6 +350,8 @@ void fill_rowwarp_args(const fos_desc *desc, int esz, int64_t row_base, int64_t 
   a->test_stall = launch ? launch->test_stall : 0;
   a->need_geo = (desc->causal || desc->kv_valid_len || desc->key_mask) ? 1 : 0;
   a->geo32 = (row_base + nrows <= (int64_t)INT32_MAX) ? 1 : 0;
+  a->qdiv = make_fastdiv((uint32_t)desc->q_len);
+  a->hdiv = make_fastdiv((uint32_t)desc->heads);
   a->err = dev.err;
 }
 

@@ -225,15 +225,21 @@ __device__ __forceinline__ void store_lane8(unsigned char *row, int j0, int L, b
 // can be valid (causal bound and valid length; key_mask and -inf
 // are applied per key), b and h its batch entry and head.  Only computed when a mask or a
 // sink needs it (one thread per row calls this, when it issues the row's copy).
+// n / d with the constants of make_fastdiv (exact for every 32-bit n).
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 __device__ __forceinline__ int4 row_geometry(const RowArgs &a, int64_t r) {
   int4 g = make_int4(a.L, 0, 0, 0);
   if (!a.need_geo) return g;
   r += a.row_base;
   int64_t b, h, i;
-  if (a.geo32) {  // 32-bit arithmetic suffices
-    const uint32_t rr = (uint32_t)r, q = rr / (uint32_t)a.q_len;
+  if (a.geo32) {  // 32-bit arithmetic suffices; the divisions are multiply-highs
+    const uint32_t rr = (uint32_t)r, q = fast_div(rr, a.qdiv);
     i = rr - q * (uint32_t)a.q_len;
-    b = q / (uint32_t)a.heads;
+    b = fast_div(q, a.hdiv);
     h = q - (uint32_t)b * (uint32_t)a.heads;
   } else {
     const int64_t q = r / a.q_len;

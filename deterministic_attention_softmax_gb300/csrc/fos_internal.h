@@ -12,6 +12,25 @@ namespace fos {
 
 constexpr int kTileK = 256;  // keys per tile: part of the arithmetic contract
 
+// n / d for 32-bit unsigned n by a multiply-high and two shifts, d fixed and at least 1:
+// Granlund and Montgomery, "Division by invariant integers using multiplication" (1994),
+// Figure 4.1.  l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, s1 = min(l, 1),
+// s2 = max(l - 1, 0); then t = mulhi(m, n) and n / d = (t + ((n - t) >> s1)) >> s2.
+struct FastDiv {
+  uint32_t m, s1, s2;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  if (d < 1) d = 1;
+  uint32_t l = 0;
+  while (l < 32 && (1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+  f.s1 = l > 0 ? 1u : 0u;
+  f.s2 = l > 0 ? l - 1 : 0u;
+  return f;
+}
+
 // Geometry and masks shared by the forward and backward row kernels.
 struct RowArgs {
   int64_t rows;                // rows of this launch
@@ -33,6 +52,7 @@ struct RowArgs {
   int32_t test_stall;          // test only: CTA 0 never issues its first copy
   int32_t need_geo;            // rows need b / h / limit (a mask or a sink is given)
   int32_t geo32;               // row_base + rows fits in int32: 32-bit geometry arithmetic
+  FastDiv qdiv, hdiv;          // 32-bit division by q_len and by heads
   unsigned *err;               // device error word
 };
 
