@@ -225,12 +225,6 @@ __device__ __forceinline__ void store_lane8(unsigned char *row, int j0, int L, b
 // can be valid (causal bound and valid length; key_mask and -inf
 // are applied per key), b and h its batch entry and head.  Only computed when a mask or a
 // sink needs it (one thread per row calls this, when it issues the row's copy).
-// n / d with the constants of make_fastdiv (exact for every 32-bit n).
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
-  const uint32_t t = __umulhi(n, f.m);
-  return (t + ((n - t) >> f.s1)) >> f.s2;
-}
-
 __device__ __forceinline__ int4 row_geometry(const RowArgs &a, int64_t r) {
   int4 g = make_int4(a.L, 0, 0, 0);
   if (!a.need_geo) return g;

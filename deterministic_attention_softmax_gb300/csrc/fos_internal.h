@@ -31,6 +31,16 @@ inline FastDiv make_fastdiv(uint32_t d) {
   return f;
 }
 
+// n / d with the constants of make_fastdiv (exact for every 32-bit n).
+__host__ __device__ inline uint32_t fast_div(uint32_t n, const FastDiv &f) {
+#if defined(__CUDA_ARCH__)
+  const uint32_t t = __umulhi(n, f.m);
+#else
+  const uint32_t t = (uint32_t)(((uint64_t)n * f.m) >> 32);
+#endif
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 // Geometry and masks shared by the forward and backward row kernels.
 struct RowArgs {
   int64_t rows;                // rows of this launch
