@@ -44,7 +44,10 @@ def vec_untouched(v, n, fill):
 
 
 @pytest.mark.parametrize("dtype_name", list(DTYPES))
-@pytest.mark.parametrize("L,ld", [(4352, 4360), (4608, 4608), (777, 781), (257, 264)])
+# 4352 / 4608: CTA kernels with e_j parked in tensor memory; 2048 / 1024 (aligned): one warp per
+# row, e_j parked; 777 / 257 (unaligned): CTA kernels with plain loads, e_j in registers
+@pytest.mark.parametrize("L,ld", [(4352, 4360), (4608, 4608), (2048, 2056), (1024, 1024),
+                                  (777, 781), (257, 264)])
 @pytest.mark.parametrize("masked", [False, True])
 def test_outputs_stay_inside_their_rows(dtype_name, L, ld, masked):
     dt = DTYPES[dtype_name]
