@@ -68,7 +68,15 @@ def test_reference_arm_prints_one_line_on_a_single_rank():
                         "--steps", "3", "--warmup", "3"],
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
-    line = json.loads(r.stdout.strip().splitlines()[-1])
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in line, key
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["config"]["workload"] == "qwen_image_bf16"
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["sample"]
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
