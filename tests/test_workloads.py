@@ -70,3 +70,49 @@ def test_padding_mean_valid_keys_is_the_mean_valid_length():
     lens = W.valid_lengths(w).numpy()
     assert ((lens >= 4096 + 32) & (lens <= 4096 + 512)).all()
     assert W.mean_valid_keys(w) == pytest.approx(brute_mean_valid(w.key_len, 3, False, lens))
+
+
+def small(**kw):
+    base = dict(name="s", dtype=torch.bfloat16, batch=2, heads=3, q_len=4, key_len=300,
+                score_sigma=4.0, seed=7)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+def test_inputs_are_reproducible_and_seeded():
+    w = small()
+    a, b = W.scores(w, "cpu"), W.scores(w, "cpu")
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    c = W.scores(w, "cpu", seed_offset=1)
+    assert not torch.equal(a, c)
+    assert not torch.equal(W.dprobs(w, "cpu"), W.dprobs(w, "cpu", seed_offset=1))
+    assert not torch.equal(W.scores(small(seed=8), "cpu"), a)
+    assert a.shape == (24, 300) and a.dtype == torch.bfloat16
+
+
+def test_inputs_are_rounded_once_from_float32():
+    # sigma * N(0,1) in float32, then one round-to-nearest-even to the dtype
+    w = small()
+    x = W.scores(w, "cpu")
+    ref = (torch.randn((24, 300), generator=torch.Generator().manual_seed(7 * 1000 + 1)) * 4.0)
+    assert torch.equal(x, ref.to(torch.bfloat16))
+
+
+def test_padding_tail_is_minus_infinity_past_each_valid_length():
+    w = small(pad=(200, 10, 60))
+    lens = W.valid_lengths(w)
+    assert lens.dtype == torch.int32 and lens.shape == (2,)
+    assert ((lens >= 210) & (lens <= 260)).all()
+    x = W.scores(w, "cpu").view(2, 12, 300)
+    for b in range(2):
+        assert torch.isneginf(x[b, :, int(lens[b]):]).all()
+        assert torch.isfinite(x[b, :, :int(lens[b])]).all()
+    assert torch.isfinite(W.scores(w, "cpu", neg_inf_tail=False)).all()
+
+
+def test_sink_logits_and_probability_inputs():
+    assert W.sink_logits(small()) is None
+    s = W.sink_logits(small(sink=True))
+    assert s.shape == (3,) and s.dtype == torch.float32
+    p = W.probs_like(small(), "cpu").float()
+    assert (p >= 0).all() and float(p.max()) <= 5.0 / 300 + 1e-6
