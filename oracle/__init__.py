@@ -13,6 +13,9 @@ them:
 * backward -- the first page's "Fixed-order backward" (the softmax VJP).
 * d_sink   -- the derivative of the rows' losses with respect to the per-head sink logit.
 
+``oracle/gemm.py`` holds the FP64 oracle of the two contractions around the softmax (QK and
+PV, with their backward products), pinned by ``tests/test_oracle_gemm.py``.
+
 All inputs are numpy arrays holding the exact stored values (bf16/fp32 widened to float64).
 Parity for every function here is pinned by ``tests/test_oracle.py`` and
 ``tests/test_golden.py`` (closed forms, invariants, finite differences, brute force).
