@@ -92,7 +92,9 @@ def test_fully_masked_rows_and_minus_inf_sink(dtype_name):
 @pytest.mark.parametrize("dtype_name", list(DTYPES))
 @pytest.mark.parametrize("L", [8193, 16384])
 def test_rows_past_the_register_path(dtype_name, L):
-    # more than 8 warps x 4 tiles: e_j and (P, dP) are recomputed / re-read from shared memory
+    # 33 and 64 tiles: the forward parks e_j in tensor memory with 5 and 8 warps (two warps share
+    # a lane quarter, side by side in its columns); the backward re-reads P and dP from shared
+    # memory
     run_and_check(dtype_name, make_case(DTYPES[dtype_name], L, "all", B=1, H=2, Sq=3))
 
 
