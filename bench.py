@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--warm-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload table (all synthetic workloads, cold medians)")
+    ap.add_argument("--workload-iters", type=int, default=20)
     ap.add_argument("--profile", choices=["fwd", "bwd", "sink"], default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
@@ -249,17 +252,17 @@ def oracle_sample(w, rows):
     return x, p, dp
 
 
-def time_oracle(w, rows, repeats):
+def time_oracle(w, rows, repeats, nthreads=0):
     import oracle
 
     x, p, dp = oracle_sample(w, rows)
-    oracle_pass(x[:2], p[:2], dp[:2], w)  # load + warm
+    oracle_pass(x[:2], p[:2], dp[:2], w, nthreads)  # load + warm
     times = []
     for _ in range(repeats):
         t0 = time.perf_counter()
-        oracle_pass(x, p, dp, w)
+        oracle_pass(x, p, dp, w, nthreads)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), oracle.max_threads()
+    return statistics.median(times), (nthreads or oracle.max_threads())
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -307,6 +310,155 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# --------------------------------------------------------------------------- all workloads
+
+# The synthetic workloads the measured metric is defined on (16,384-row Qwen-Image rows at
+# 4,352 keys, padded prompts, causal rows with a sink, the large bf16 / fp32 case, the tiny
+# fp32 case); the headline `value` is the first.
+REPORTED = ["qwen_image_bf16", "prompt_padding_bf16", "sink_causal_bf16", "large_bf16",
+            "large_fp32", "tiny_fp32"]
+
+
+def sha256_rows(*tensors, rows=None):
+    """SHA-256 of the raw bytes of the tensors (their first `rows` rows when given)."""
+    h = hashlib.sha256()
+    for t in tensors:
+        t = t if rows is None else t[:rows]
+        h.update(t.contiguous().view(-1).view(__import__("torch").uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+def parity_gate(fos, w, dev, x, dp, p, lse, kv, sink, nrows=32):
+    """Sampled rows of the workload against the FP64 oracle: the forward's P and LSE on the
+    rows as they sit in the batch (their masks and sink), then the backward of those rows on the
+    oracle's own P rounded to the dtype.  Returns (ok, detail)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from oracle import tolerance as tol
+
+    ids = np.unique(np.concatenate([[0, w.rows - 1],
+                                    np.random.default_rng(0).integers(0, w.rows, nrows)]))
+    ids_d = torch.from_numpy(ids).to(dev)
+    okw = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal,
+               kv_valid_len=None if kv is None else kv.cpu().numpy(), row_ids=ids)
+    xs = x.index_select(0, ids_d).double().cpu().numpy()
+    p_ref, lse_ref = oracle.softmax_fwd(
+        xs, sink=None if sink is None else sink.double().cpu().numpy(), **okw)
+    dname = str(w.dtype).replace("torch.", "")
+    r_p = tol.check_probs(p.index_select(0, ids_d).double().cpu().numpy(), p_ref, dname)
+    r_l = tol.check_lse(lse.index_select(0, ids_d).double().cpu().numpy(), lse_ref)
+    # the sampled rows' P is 0 on their masked keys already, so they run as unmasked rows
+    p_in = torch.from_numpy(p_ref).to(w.dtype).to(dev)
+    dps = dp.index_select(0, ids_d).contiguous()
+    ds_s, delta_s = fos.fos_softmax_bwd(p_in, dps, q_len=len(ids))
+    pin, dpn = p_in.double().cpu().numpy(), dps.double().cpu().numpy()
+    ds_ref, delta_ref = oracle.softmax_bwd(pin, dpn, batch=1, heads=1, q_len=len(ids))
+    r_d = tol.check_dscores(ds_s.double().cpu().numpy(), ds_ref, pin, dpn, dname)
+    r_dl = tol.check_delta(delta_s.double().cpu().numpy(), delta_ref, pin, dpn)
+    ok = r_p[0] and r_l[0] and r_d[0] and r_dl[0]
+    detail = {"rows": int(len(ids)), "worst_err_over_bound": {
+        "P": round(r_p[1], 4), "LSE": round(r_l[1], 4), "dS": round(r_d[1], 4),
+        "delta": round(r_dl[1], 4)}}
+    return ok, detail
+
+
+def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
+    """One workload: inputs resident in HBM, a parity gate, then per-kernel CUDA-event medians.
+    `cold`: a 512 MB scratch write (4x the L2) before each kernel, so every kernel reads its
+    inputs from DRAM (its own writes still drain after its end event).  `step`: fwd + bwd
+    (+ sink gradient) back to back, no flush, one input set (more than L2 except for the tiny
+    workload)."""
+    import torch
+
+    from deterministic_attention_softmax_gb300 import workloads as W
+
+    kv = W.valid_lengths(w)
+    kv = None if kv is None else kv.to(dev)
+    sink = W.sink_logits(w)
+    sink = None if sink is None else sink.to(dev)
+    geo = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal, kv_valid_len=kv)
+    x = W.scores(w, dev)
+    dp = W.dprobs(w, dev)
+    p = torch.empty_like(x)
+    ds = torch.empty_like(x)
+    lse = torch.empty(w.rows, dtype=torch.float32, device=dev)
+    delta = torch.empty(w.rows, dtype=torch.float32, device=dev)
+    d_sink = torch.empty(w.heads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        fos.fos_softmax_fwd(x, p, lse, sink=sink, **geo)
+
+    def bwd():
+        fos.fos_softmax_bwd(p, dp, ds, delta, **geo)
+
+    def sgrad():
+        fos.fos_sink_grad(lse, delta, sink, d_sink, batch=w.batch, heads=w.heads, q_len=w.q_len)
+
+    fwd()
+    ok, gate = parity_gate(fos, w, dev, x, dp, p, lse, kv, sink)
+    if not ok:
+        raise SystemExit(f"parity gate failed before timing on {w.name}: {gate}")
+    kernels = [("fwd", fwd), ("bwd", bwd)] + ([("sink", sgrad)] if sink is not None else [])
+    scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    cold = {k: [] for k, _ in kernels}
+    for it in range(warmup + iters):
+        for name, f in kernels:
+            scratch.fill_(it & 0xff)
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            if it >= warmup:
+                cold[name].append((e0, e1))
+    steps = []
+    for it in range(warmup + iters):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _, f in kernels:
+            f()
+        e1.record(stream)
+        if it >= warmup:
+            steps.append((e0, e1))
+    torch.cuda.synchronize()
+    if fos.fos_device_error() != 0:
+        raise SystemExit(f"device error while timing {w.name}")
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in cold.items()}
+    step_ms = statistics.median(a.elapsed_time(b) for a, b in steps)
+    vk = W.mean_valid_keys(w)
+    b = W.algorithmic_bytes(w, valid_keys=vk)
+    gbs = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+    tot = b["fwd"] + b["bwd"] + b["sink"]
+    cold_sum = sum(med.values())
+    out = {
+        "rows": w.rows, "key_len": w.key_len, "dtype": str(w.dtype).replace("torch.", ""),
+        "mean_valid_keys": vk, "parity_gate": dict(gate, result="pass"),
+        "fwd_cold_ms": med["fwd"], "bwd_cold_ms": med["bwd"],
+        "sink_cold_ms": med.get("sink"),
+        "fwd_gbs": gbs(b["fwd"], med["fwd"]), "bwd_gbs": gbs(b["bwd"], med["bwd"]),
+        "fwd_bwd_gbs": gbs(tot, cold_sum),
+        "fwd_frac": gbs(b["fwd"], med["fwd"]) / peak,
+        "bwd_frac": gbs(b["bwd"], med["bwd"]) / peak,
+        "fwd_bwd_frac": gbs(tot, cold_sum) / peak,
+        "step_ms": step_ms, "step_gbs": gbs(tot, step_ms), "step_frac": gbs(tot, step_ms) / peak,
+        "rows_per_s_fwd": w.rows / (med["fwd"] * 1e-3),
+        "rows_per_s_fwd_bwd": w.rows / (cold_sum * 1e-3),
+        "algorithmic_bytes": {k: b[k] for k in ("fwd", "bwd", "sink")},
+        "input_sha256_first_1024_rows": sha256_rows(x, dp, rows=1024),
+        "timing": f"medians of {iters} launches per kernel after {warmup} warm-up; cold = "
+                  f"512 MB scratch write before each kernel; step = kernels back to back",
+    }
+    del x, dp, p, ds, scratch
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- our arm
 
 
@@ -346,34 +498,11 @@ def run_ours(args):
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0].values())
 
     # ---- parity gate before timing: sampled rows of set 0 against the oracle
-    import numpy as np
-
-    import oracle
-    from oracle import tolerance as tol
-
     s0 = sets[0]
     fos.fos_softmax_fwd(s0["x"], s0["p"], s0["lse"], sink=sink, **geo)
-    ids = np.unique(np.concatenate([[0, w.rows - 1], np.random.default_rng(0).integers(0, w.rows, 30)]))
-    ids_d = torch.from_numpy(ids).to(dev)
-    xs = s0["x"].index_select(0, ids_d).double().cpu().numpy()
-    okw = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal,
-               kv_valid_len=None if kv is None else kv.cpu().numpy(), row_ids=ids)
-    p_ref, lse_ref = oracle.softmax_fwd(xs, sink=None if sink is None else sink.double().cpu().numpy(),
-                                        **okw)
-    dname = str(w.dtype).replace("torch.", "")
-    ok_p = tol.check_probs(s0["p"].index_select(0, ids_d).double().cpu().numpy(), p_ref, dname)[0]
-    ok_l = tol.check_lse(s0["lse"].index_select(0, ids_d).double().cpu().numpy(), lse_ref)[0]
-    # backward gate on the sampled rows alone (as rows of one head, no mask: their P is 0 on
-    # masked keys already)
-    p_in = torch.from_numpy(p_ref).to(w.dtype).to(dev)
-    dps = s0["dp"].index_select(0, ids_d).contiguous()
-    ds_s, delta_s = fos.fos_softmax_bwd(p_in, dps, q_len=len(ids))
-    ds_ref, delta_ref = oracle.softmax_bwd(p_in.double().cpu().numpy(), dps.double().cpu().numpy(),
-                                           batch=1, heads=1, q_len=len(ids))
-    ok_d = tol.check_dscores(ds_s.double().cpu().numpy(), ds_ref, p_in.double().cpu().numpy(),
-                             dps.double().cpu().numpy(), dname)[0]
-    if not (ok_p and ok_l and ok_d):
-        raise SystemExit(f"parity gate failed before timing: P {ok_p} LSE {ok_l} dS {ok_d}")
+    ok, gate = parity_gate(fos, w, dev, s0["x"], s0["dp"], s0["p"], s0["lse"], kv, sink)
+    if not ok:
+        raise SystemExit(f"parity gate failed before timing: {gate}")
 
     # ---- launch arguments prebuilt once (the timed loop is two C calls per step)
     kvp = None if kv is None else kv.data_ptr()
@@ -428,9 +557,11 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier(pg)
     total_ms = start.elapsed_time(end)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    sink_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) if sink is not None else 0.0
+    fwd_all = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_all = [e[1].elapsed_time(e[2]) for e in evs]
+    fwd_ms, bwd_ms = statistics.median(fwd_all), statistics.median(bwd_all)
+    fwd_mean, bwd_mean = statistics.mean(fwd_all), statistics.mean(bwd_all)
+    sink_ms = statistics.median(e[2].elapsed_time(e[3]) for e in evs) if sink is not None else 0.0
     assert fos.fos_device_error() == 0
     ms_step_rank = total_ms / K
     ms_step = max_over_ranks(pg, ms_step_rank, dev)
@@ -473,6 +604,17 @@ def run_ours(args):
                 "steps": args.warm_steps, "inputs": f"one set of {set_bytes / 1e9:.2f} GB reused"}
         assert fos.fos_device_error() == 0
     p0 = hbm_probe(dev)
+    in_sha = sha256_rows(sets[0]["x"], sets[0]["dp"])
+
+    # ---- every synthetic workload, cold per-kernel medians (after the headline's timed region)
+    table = None
+    if not args.no_workloads and rank == 0:
+        table = {}
+        with ClockSampler(local) as wclk:
+            for name in REPORTED:
+                table[name] = measure_workload(fos, W.WORKLOADS[name], dev, peak,
+                                               iters=args.workload_iters)
+        table["clocks"] = wclk.summary()
 
     # ---- end to end through the public Python API with pinned host buffers
     e2e = None
@@ -519,9 +661,13 @@ def run_ours(args):
         rows = 2048
         t, cores = time_oracle(w, rows, 3)
         cpu_gbs = (step_bytes / w.rows) * rows / t / 1e9
+        t1, _ = time_oracle(w, 256, 3, nthreads=1)
         cpu = {"value": cpu_gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{rows} rows of {w.name}, fwd+bwd, FP64 C oracle, median of 3",
-               "rows_per_s": rows / t}
+               "rows_per_s": rows / t,
+               "one_core": {"value": (step_bytes / w.rows) * 256 / t1 / 1e9, "unit": "GB/s",
+                            "rows_per_s": 256 / t1,
+                            "sample": f"256 rows of {w.name}, fwd+bwd, one thread, median of 3"}}
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -536,13 +682,18 @@ def run_ours(args):
                             (" + fos_sink_grad" if sink is not None else ""),
                        mean_valid_keys=vk),
         "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "fwd_ms_mean": fwd_mean, "bwd_ms_mean": bwd_mean,
+        "per_kernel_timing": "medians of the K timed steps' CUDA events (back to back, "
+                             "rotating input sets: each kernel also drains the previous one's "
+                             "writes; see workloads for cold per-kernel numbers)",
+        "input_sha256": in_sha,
         "sink_ms": sink_ms if sink is not None else None,
         "fwd_bwd_frac_of_peak": value / world / peak,
         "rows_per_s_fwd": w.rows / (fwd_ms * 1e-3) * world,
         "rows_per_s_fwd_bwd": w.rows / (ms_step * 1e-3) * world,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch * K,
-        "clocks": clocks, "parity_gate": "sampled rows vs FP64 oracle: pass",
-        "warm": warm, "p0_hbm_probe": p0,
+        "clocks": clocks, "parity_gate": dict(gate, result="pass"),
+        "warm": warm, "p0_hbm_probe": p0, "workloads": table,
     }
     print(json.dumps(line))
 

@@ -98,6 +98,35 @@ def test_rows_past_the_register_path(dtype_name, L):
     run_and_check(dtype_name, make_case(DTYPES[dtype_name], L, "all", B=1, H=2, Sq=3))
 
 
+@pytest.mark.parametrize("dtype_name", list(DTYPES))
+@pytest.mark.parametrize("L", [16385, 24576, 32768])
+def test_widest_parked_forward_layout(dtype_name, L):
+    # 65, 96 and 128 tiles on the default launch: the CTA forward takes 9, 12 and 16 compute
+    # warps with 8 tiles each parked in tensor memory, so up to four warps share a lane quarter
+    # side by side in its columns (256 columns per CTA).  Every mask kind and a sink; 18 rows.
+    run_and_check(dtype_name, make_case(DTYPES[dtype_name], L, "all", B=2, H=3, Sq=3))
+
+
+@pytest.mark.parametrize("dtype_name", list(DTYPES))
+@pytest.mark.parametrize("L", [18432, 32768])
+@pytest.mark.parametrize("mask", ["none", "all"])
+def test_wide_layouts_match_the_recompute_path(dtype_name, L, mask):
+    # 72 and 128 tiles over 9, 12 and 16 warps: at 72 tiles every count parks e_j (8, 6 and 6
+    # tiles per warp: three, three and four warps per lane quarter); at 128 tiles 16 warps park
+    # 8 each while 9 and 12 warps recompute e_j in the second pass.  Eight warps (9 and 16
+    # tiles per warp) recompute in both.  All must give the same bits, for the instance
+    # specialised for unmasked rows and for the general one.
+    c = make_case(DTYPES[dtype_name], L, mask, B=2, H=2, Sq=4)
+    kw = dict(batch=c["B"], heads=c["H"], q_len=c["Sq"], causal=c["causal"],
+              kv_valid_len=c["kv"], key_mask=c["km"], sink=c["sink"])
+    ref = fos.fos_softmax_fwd(c["x"], launch=fos.Launch(warps_per_cta=8), **kw)
+    for warps in (9, 12, 16):
+        out = fos.fos_softmax_fwd(c["x"], launch=fos.Launch(warps_per_cta=warps), **kw)
+        assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1]), warps
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+
+
 @pytest.mark.parametrize("dtype_name,L_fwd,L_bwd", [("float32", 57000, 28672),
                                                     ("bfloat16", 100000, 57344),
                                                     ("float16", 100000, 57344)])

@@ -4,6 +4,8 @@
 Two calls in a row through the C ABI, on one stream and without a synchronisation between
 them, must each give what the workspace-taking entry point (fos_softmax_step_host) gives for
 the same inputs: the same bits, which is tighter than the oracle tolerance of the parity tests.
+Between the two, a call of another dtype and row length fills the array with other bytes, so
+the second call also shows that nothing in the array has to start at zero.
 Problems whose scratch would not fit are refused with FOS_ERR_UNSUPPORTED before anything is
 enqueued.  This file is collected last, and it builds the library itself so that it also runs
 alone in a fresh process."""
@@ -59,12 +61,26 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(lib):
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     ins = [host_inputs(seed) for seed in (1, 2)]
     outs = [host_outputs() for _ in ins]
-    for (x, dp), o in zip(ins, outs):  # back to back on one stream
+    # the call in between: float32 rows of 3000 keys, another chunk layout in the array
+    rows_f, L_f = 1536, 3000
+    g = torch.Generator().manual_seed(4)
+    xf = (torch.randn(rows_f, L_f, generator=g) * 4).pin_memory()
+    dpf = torch.randn(rows_f, L_f, generator=g).pin_memory()
+    of = dict(p=torch.empty_like(xf).pin_memory(), ds=torch.empty_like(xf).pin_memory(),
+              lse=torch.empty(rows_f).pin_memory(), delta=torch.empty(rows_f).pin_memory())
+    desc_f = _abi.FosDesc(rows_f, L_f, L_f, 1, 1, rows_f, 0, 0, None, None, None)
+    calls = [(desc, _abi.FOS_BF16, ins[0], outs[0]), (desc_f, _abi.FOS_F32, (xf, dpf), of),
+             (desc, _abi.FOS_BF16, ins[1], outs[1])]
+    for d, dt, (x, dp), o in calls:  # back to back on one stream
         st = lib.fos_softmax_step_host_static(
-            ctypes.byref(desc), _abi.FOS_BF16, ptr(x), ptr(dp), ptr(o["p"]), ptr(o["lse"]),
-            ptr(o["ds"]), ptr(o["delta"]), ptr(o["d_sink"]), 0, stream, None)
+            ctypes.byref(d), dt, ptr(x), ptr(dp), ptr(o["p"]), ptr(o["lse"]), ptr(o["ds"]),
+            ptr(o["delta"]), ptr(o["d_sink"]) if "d_sink" in o else None, 0, stream, None)
         assert st == _abi.FOS_OK, lib.fos_status_string(st)
     torch.cuda.synchronize()
+    ref_f = fos.fos_softmax_step_host(xf, dpf, batch=1, heads=1, q_len=rows_f)
+    torch.cuda.synchronize()
+    for got, want in zip((of["p"], of["lse"], of["ds"], of["delta"]), ref_f):
+        assert torch.equal(bits(got), bits(want))
     geo = dict(batch=B, heads=H, q_len=SQ, causal=True, kv_valid_len=kv)
     for (x, dp), o in zip(ins, outs):
         ref = fos.fos_softmax_step_host(x, dp, sink=sink, **geo)
