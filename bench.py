@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
     ap.add_argument("--workload-iters", type=int, default=20)
-    ap.add_argument("--profile", choices=["fwd", "bwd", "sink"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk"], default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
     return ap.parse_args()
@@ -366,8 +366,9 @@ def parity_gate(fos, w, dev, x, dp, p, lse, kv, sink, nrows=32):
 
 def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
     """One workload: inputs resident in HBM, a parity gate, then per-kernel CUDA-event medians.
-    `cold`: a 512 MB scratch write (4x the L2) before each kernel, so every kernel reads its
-    inputs from DRAM (its own writes still drain after its end event).  `step`: fwd + bwd
+    `cold`: a 512 MB scratch read (4x the L2) before each kernel, so every kernel reads its
+    inputs from DRAM and finds no dirty line of another kernel in L2 (its own writes still
+    drain after its end event).  `step`: fwd + bwd
     (+ sink gradient) back to back, no flush, one input set (more than L2 except for the tiny
     workload)."""
     import torch
@@ -388,29 +389,64 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
     d_sink = torch.empty(w.heads, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the timed calls go straight to the C ABI with their arguments built once, so no Python
+    # work sits between a kernel's start and end events
+    from deterministic_attention_softmax_gb300 import _abi
+
+    lib = _abi.lib()
+    dt = {torch.float32: _abi.FOS_F32, torch.bfloat16: _abi.FOS_BF16,
+          torch.float16: _abi.FOS_F16}[w.dtype]
+    desc = _abi.FosDesc(w.rows, w.key_len, w.key_len, w.batch, w.heads, w.q_len, int(w.causal), 0,
+                        None if kv is None else kv.data_ptr(), None,
+                        None if sink is None else sink.data_ptr())
+    dref = ctypes.byref(desc)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    vp = ctypes.c_void_p
+    ws = None
+    if sink is not None:
+        ws = torch.empty(max(1, lib.fos_bwd_sink_workspace_bytes(dref)), dtype=torch.uint8,
+                         device=dev)
+
+    def call(st, what):
+        if st != _abi.FOS_OK:
+            raise SystemExit(f"{what} failed with status {st} on {w.name}")
+
     def fwd():
-        fos.fos_softmax_fwd(x, p, lse, sink=sink, **geo)
+        call(lib.fos_softmax_fwd(dref, dt, vp(x.data_ptr()), vp(p.data_ptr()),
+                                 vp(lse.data_ptr()), sh, None), "fwd")
 
     def bwd():
-        fos.fos_softmax_bwd(p, dp, ds, delta, **geo)
+        call(lib.fos_softmax_bwd(dref, dt, vp(p.data_ptr()), vp(dp.data_ptr()),
+                                 vp(ds.data_ptr()), vp(delta.data_ptr()), sh, None), "bwd")
 
     def sgrad():
-        fos.fos_sink_grad(lse, delta, sink, d_sink, batch=w.batch, heads=w.heads, q_len=w.q_len)
+        call(lib.fos_sink_grad(dref, vp(lse.data_ptr()), vp(delta.data_ptr()),
+                               vp(d_sink.data_ptr()), sh, None), "sink")
+
+    def bwd_sink():  # the backward with the sink gradient taken along (no delta written)
+        call(lib.fos_softmax_bwd_sink(dref, dt, vp(p.data_ptr()), vp(dp.data_ptr()),
+                                      vp(ds.data_ptr()), None, vp(lse.data_ptr()),
+                                      vp(d_sink.data_ptr()), vp(ws.data_ptr()),
+                                      ws.numel(), sh, None), "bwd_sink")
 
     fwd()
     ok, gate = parity_gate(fos, w, dev, x, dp, p, lse, kv, sink)
     if not ok:
         raise SystemExit(f"parity gate failed before timing on {w.name}: {gate}")
     kernels = [("fwd", fwd), ("bwd", bwd)] + ([("sink", sgrad)] if sink is not None else [])
-    scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    extra = [("bwd_sink", bwd_sink)] if sink is not None else []
+    # L2 flush between launches: a READ of 512 MB (4x the L2), so that the timed kernel finds
+    # only clean, unrelated lines in L2 (a write would leave dirty lines whose write-back the
+    # next kernel would pay for)
+    scratch = torch.ones(128 << 20, dtype=torch.float32, device=dev)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    cold = {k: [] for k, _ in kernels}
+    cold = {k: [] for k, _ in kernels + extra}
     for it in range(warmup + iters):
-        for name, f in kernels:
-            scratch.fill_(it & 0xff)
+        for name, f in kernels + extra:
+            scratch.sum()
             e0, e1 = ev(), ev()
             e0.record(stream)
             f()
@@ -430,6 +466,7 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
     if fos.fos_device_error() != 0:
         raise SystemExit(f"device error while timing {w.name}")
     med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in cold.items()}
+    fused = med.pop("bwd_sink", None)
     step_ms = statistics.median(a.elapsed_time(b) for a, b in steps)
     vk = W.mean_valid_keys(w)
     b = W.algorithmic_bytes(w, valid_keys=vk)
@@ -451,10 +488,92 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
         "rows_per_s_fwd_bwd": w.rows / (cold_sum * 1e-3),
         "algorithmic_bytes": {k: b[k] for k in ("fwd", "bwd", "sink")},
         "input_sha256_first_1024_rows": sha256_rows(x, dp, rows=1024),
+        "bwd_with_sink_fused_cold_ms": fused,
+        "bwd_then_sink_cold_ms": (med["bwd"] + med["sink"]) if fused is not None else None,
         "timing": f"medians of {iters} launches per kernel after {warmup} warm-up; cold = "
-                  f"512 MB scratch write before each kernel; step = kernels back to back",
+                  f"512 MB scratch read before each kernel; step = kernels back to back",
     }
-    del x, dp, p, ds, scratch
+    del x, dp, p, ds, scratch, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
+    """The QK contraction that produces the benchmark's scores: 16,384 query rows (4 heads x
+    4,096) against 4,352 keys, head dimension 128, bf16 Q and K, float32 and bf16 scores.  A
+    parity gate on sampled query rows, then cold CUDA-event medians (512 MB scratch read before
+    each launch).  Roofline: HBM (the score writes dominate: 64 flops per float32 score byte,
+    far below the tensor cores' ratio), with the tensor-core rate reported beside it."""
+    import numpy as np
+    import torch
+
+    from oracle import gemm
+    from oracle import tolerance as tol
+
+    B, H, Sq, Skv, D = 1, 4, 4096, 4352, 128
+    g = torch.Generator(device=dev).manual_seed(61)
+    q = torch.randn(B, H, Sq, D, generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(B, H, Skv, D, generator=g, device=dev).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    scratch = torch.ones(128 << 20, dtype=torch.float32, device=dev)  # read-only L2 flush
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    tflops_peak = float(peaks.get("bf16_tflops", 1900.0))
+    out = {"shape": {"batch": B, "heads": H, "q_len": Sq, "kv_len": Skv, "head_dim": D},
+           "flops_per_launch": 2.0 * B * H * Sq * Skv * D}
+    for odt in (torch.float32, torch.bfloat16):
+        s = fos.fos_qk_scores(q, k, scale, out_dtype=odt)
+        rows = np.unique(np.concatenate([[0, Sq - 1],
+                                         np.random.default_rng(1).integers(0, Sq, 24)]))
+        r = torch.from_numpy(rows).to(dev)
+        qn = q[:, :, r].double().cpu().numpy()
+        kn = k.double().cpu().numpy()
+        ref = gemm.qk_scores(qn, kn, scale)
+        absd = gemm.qk_scores(np.abs(qn), np.abs(kn), 1.0)
+        name = str(odt).replace("torch.", "")
+        ok, worst, _ = tol.check_scores(s[:, :, r].double().cpu().numpy(), ref, absd, scale, name)
+        if not ok:
+            raise SystemExit(f"QK parity gate failed ({name}): worst {worst}")
+        nbytes = q.numel() * 2 + k.numel() * 2 + s.numel() * s.element_size()
+        res = {"algorithmic_bytes": nbytes,
+               "parity_gate": {"rows": int(len(rows)), "worst_err_over_bound": worst}}
+        from deterministic_attention_softmax_gb300 import _abi
+
+        lib = _abi.lib()
+        odt_c = {torch.float32: _abi.FOS_F32, torch.bfloat16: _abi.FOS_BF16}[odt]
+        sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        qp, kp, sp_ = (ctypes.c_void_p(t.data_ptr()) for t in (q, k, s))
+        for tile_n in (0, 256):  # the default (128 keys per tile), then 256
+            d = _abi.FosQkDesc(B, H, H, Sq, Skv, D, s.stride(2), scale, tile_n)
+            dr = ctypes.byref(d)
+            evs = []
+            for it in range(warmup + iters):
+                scratch.sum()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if lib.fos_qk_scores(dr, _abi.FOS_BF16, odt_c, qp, kp, sp_, sh) != _abi.FOS_OK:
+                    raise SystemExit("fos_qk_scores failed while timing")
+                e1.record()
+                if it >= warmup:
+                    evs.append((e0, e1))
+            torch.cuda.synchronize()
+            if fos.fos_device_error() != 0:
+                raise SystemExit("device error while timing the QK contraction")
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            r_ = {"cold_ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                  "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                  "tflops": out["flops_per_launch"] / (ms * 1e-3) / 1e12,
+                  "frac_of_bf16_tensor": out["flops_per_launch"] / (ms * 1e-3) / 1e12 /
+                  tflops_peak}
+            if tile_n == 0:
+                res.update(r_)
+                res["tile_n"] = 128
+            else:
+                res["tile_n_256"] = r_
+        out[name] = res
+        del s
+    del q, k, scratch
     torch.cuda.empty_cache()
     return out
 
@@ -614,6 +733,7 @@ def run_ours(args):
             for name in REPORTED:
                 table[name] = measure_workload(fos, W.WORKLOADS[name], dev, peak,
                                                iters=args.workload_iters)
+            table["qk_scores_qwen_image"] = measure_qk(fos, dev, peak, iters=args.workload_iters)
         table["clocks"] = wclk.summary()
 
     # ---- end to end through the public Python API with pinned host buffers
@@ -709,6 +829,16 @@ def run_profile(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fos.build()
+    if args.profile == "qk":  # the QK contraction on the Qwen-Image shape (float32 scores)
+        g = torch.Generator(device=dev).manual_seed(61)
+        q = torch.randn(1, 4, 4096, 128, generator=g, device=dev).to(torch.bfloat16)
+        k = torch.randn(1, 4, 4352, 128, generator=g, device=dev).to(torch.bfloat16)
+        s = fos.fos_qk_scores(q, k, 0.0884)
+        for _ in range(args.warmup + args.steps):
+            fos.fos_qk_scores(q, k, 0.0884, scores=s)
+        torch.cuda.synchronize()
+        assert fos.fos_device_error() == 0
+        return
     w = W.WORKLOADS[args.workload]
     kv = W.valid_lengths(w)
     kv = None if kv is None else kv.to(dev)
@@ -729,6 +859,8 @@ def run_profile(args):
             fos.fos_softmax_fwd(x, p, lse, sink=sink, **geo)
         elif args.profile == "bwd":
             fos.fos_softmax_bwd(p, dp, ds, delta, **geo)
+        elif args.profile == "bwd_sink":
+            fos.fos_softmax_bwd_sink(p, dp, lse, sink, ds, d_sink, **geo)
         else:
             fos.fos_sink_grad(lse, delta, sink, d_sink, batch=w.batch, heads=w.heads,
                               q_len=w.q_len)

@@ -11,19 +11,25 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libfos_softmax.so")
+# FOS_LIBRARY=debug selects the build whose kernels check their indices (FOS_DEBUG); it is
+# built on demand by ``_build.build(debug=True)`` and used by the tests only.
+DEBUG_LIB_PATH = os.path.join(_PKG, "libfos_softmax_debug.so")
+LIB_PATH = DEBUG_LIB_PATH if os.environ.get("FOS_LIBRARY") == "debug" else \
+    os.path.join(_PKG, "libfos_softmax.so")
 
 # fos_dtype
 FOS_F32, FOS_BF16, FOS_F16 = 0, 1, 2
 # fos_status
 FOS_OK, FOS_ERR_INVALID, FOS_ERR_UNSUPPORTED, FOS_ERR_CUDA, FOS_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FOS_ERR_INDEX = 5
 STATUS_NAMES = {0: "FOS_OK", 1: "FOS_ERR_INVALID", 2: "FOS_ERR_UNSUPPORTED", 3: "FOS_ERR_CUDA",
-                4: "FOS_ERR_TIMEOUT"}
+                4: "FOS_ERR_TIMEOUT", 5: "FOS_ERR_INDEX"}
 
 # Every symbol include/fos_softmax.h declares.
 EXPORTED = ("fos_softmax_fwd", "fos_softmax_bwd", "fos_sink_grad", "fos_sink_grad_partials",
             "fos_sink_grad_merge", "fos_softmax_step_host",
-            "fos_step_host_workspace_bytes", "fos_softmax_step_host_static", "fos_device_error",
+            "fos_step_host_workspace_bytes", "fos_softmax_step_host_static", "fos_qk_scores",
+            "fos_softmax_bwd_sink", "fos_bwd_sink_workspace_bytes", "fos_device_error",
             "fos_status_string", "fos_contract_fingerprint")
 
 
@@ -43,6 +49,20 @@ class FosDesc(ctypes.Structure):
     ]
 
 
+class FosQkDesc(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("q_heads", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
+        ("kv_len", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("ld_scores", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+        ("tile_n", ctypes.c_int32),
+    ]
+
+
 class FosLaunch(ctypes.Structure):
     _fields_ = [
         ("warps_per_cta", ctypes.c_int32),
@@ -52,6 +72,7 @@ class FosLaunch(ctypes.Structure):
         ("wait_timeout_ns", ctypes.c_int64),
         ("test_stall", ctypes.c_int32),
         ("generic", ctypes.c_int32),
+        ("groups_per_cta", ctypes.c_int32),
     ]
 
 
@@ -92,6 +113,14 @@ def lib() -> ctypes.CDLL:
         L.fos_softmax_step_host_static.argtypes = [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
                                                    ctypes.c_int64, vp, lp]
         L.fos_softmax_step_host_static.restype = ctypes.c_int
+        L.fos_softmax_bwd_sink.argtypes = [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                           ctypes.c_size_t, vp, lp]
+        L.fos_softmax_bwd_sink.restype = ctypes.c_int
+        L.fos_bwd_sink_workspace_bytes.argtypes = [dp]
+        L.fos_bwd_sink_workspace_bytes.restype = ctypes.c_size_t
+        L.fos_qk_scores.argtypes = [ctypes.POINTER(FosQkDesc), ctypes.c_int, ctypes.c_int, vp, vp,
+                                    vp, vp]
+        L.fos_qk_scores.restype = ctypes.c_int
         L.fos_device_error.argtypes = [vp]
         L.fos_device_error.restype = ctypes.c_int
         L.fos_status_string.argtypes = [ctypes.c_int]

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfos_softmax.so")
-SOURCES = ["fos_api.cu", "fos_fwd.cu", "fos_bwd.cu", "fos_sink.cu", "fos_host.cu"]
+SOURCES = ["fos_api.cu", "fos_fwd.cu", "fos_bwd.cu", "fos_sink.cu", "fos_host.cu", "fos_qk.cu"]
 HEADERS = [os.path.join(CSRC, "fos_device.cuh"), os.path.join(CSRC, "fos_internal.h"),
            os.path.join(ROOT, "include", "fos_softmax.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,24 +33,31 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is needed to build libfos_softmax")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+DEBUG_LIB = os.path.join(PKG, "libfos_softmax_debug.so")
+
+
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False) -> str:
-    """Compile and link the library if needed; returns its path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, debug: bool = False) -> str:
+    """Compile and link the library if needed; returns its path.  ``debug`` builds the variant
+    whose kernels check their indices (FOS_DEBUG) as ``libfos_softmax_debug.so`` instead."""
+    lib = DEBUG_LIB if debug else LIB
+    if not force and not _stale(lib):
+        return lib
+    bdir = BUILD + ("_debug" if debug else "")
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
+    extra = ["-DFOS_DEBUG"] if debug else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
@@ -58,16 +65,16 @@ def build(force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(bdir, "ptxas.log"), "w") as f:
         for obj, log in results:
             f.write(f"== {os.path.basename(obj)}\n{log}\n")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

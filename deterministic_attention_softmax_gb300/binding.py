@@ -44,10 +44,12 @@ class Launch:
     wait_timeout_ns: int = 0
     test_stall: int = 0
     generic: int = 0  # 1: never the kernel specialised for the common case
+    groups_per_cta: int = 0  # forward row groups per CTA (0: chosen by the library)
 
     def _c(self) -> _abi.FosLaunch:
         return _abi.FosLaunch(self.warps_per_cta, self.ctas, self.stages, self.load_path,
-                              self.wait_timeout_ns, self.test_stall, self.generic)
+                              self.wait_timeout_ns, self.test_stall, self.generic,
+                              self.groups_per_cta)
 
 
 def _rows_layout(t: torch.Tensor, name: str):
@@ -189,6 +191,51 @@ def fos_softmax_bwd(probs, dprobs, dscores=None, delta=None, *, batch=None, head
     if st != _abi.FOS_OK:
         raise FosError(st, "fos_softmax_bwd")
     return dscores, delta
+
+
+def fos_softmax_bwd_sink(probs, dprobs, lse, sink, dscores=None, d_sink=None, delta=None, *,
+                         batch=None, heads=None, q_len=None, causal=False, kv_valid_len=None,
+                         key_mask=None, workspace=None, stream=None,
+                         launch: Launch | None = None):
+    """Backward and sink gradient in one call (the sink gradient taken along by the backward
+    where its kernels allow, otherwise the two launches; the same bits either way).  Returns
+    ``(dscores, d_sink, delta)``; delta is written only when given."""
+    if probs.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {probs.dtype}")
+    dev = probs.device
+    rows, L, ld, batch, heads, q_len = _geometry(probs, batch, heads, q_len)
+    _same_layout(probs, dprobs, "probs", "dprobs")
+    if dscores is None:
+        dscores = _like(probs)
+    _same_layout(probs, dscores, "probs", "dscores")
+    for t, n in ((lse, "lse"), (delta, "delta")):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != rows or
+                              not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous float32 tensor with one entry per row")
+    if sink is None:
+        raise ValueError("sink is required")
+    if d_sink is None:
+        d_sink = torch.empty(heads, dtype=torch.float32, device=dev)
+    if d_sink.dtype != torch.float32 or d_sink.numel() != heads or not d_sink.is_contiguous():
+        raise ValueError("d_sink must be a contiguous float32 tensor [heads]")
+    for t, n in ((probs, "probs"), (dprobs, "dprobs"), (dscores, "dscores"), (lse, "lse"),
+                 (delta, "delta"), (sink, "sink"), (d_sink, "d_sink"),
+                 (kv_valid_len, "kv_valid_len"), (key_mask, "key_mask"), (workspace, "workspace")):
+        _check_cuda(t, n, dev)
+    d = _desc(rows, L, ld, batch, heads, q_len, causal, kv_valid_len, key_mask, sink)
+    need = int(_abi.lib().fos_bwd_sink_workspace_bytes(ctypes.byref(d)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    lc = None if launch is None else ctypes.byref(launch._c())
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_softmax_bwd_sink(
+            ctypes.byref(d), _DTYPES[probs.dtype], _ptr(probs), _ptr(dprobs), _ptr(dscores),
+            _ptr(delta), _ptr(lse), _ptr(d_sink), _ptr(workspace), ws_bytes,
+            _stream_handle(stream, dev), lc)
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_softmax_bwd_sink")
+    return dscores, d_sink, delta
 
 
 def fos_sink_grad(lse, delta, sink, d_sink=None, *, batch, heads, q_len, key_len=1,
@@ -348,6 +395,45 @@ def fos_softmax_step_host(scores, dprobs, probs=None, lse=None, dscores=None, de
     if st != _abi.FOS_OK:
         raise FosError(st, "fos_softmax_step_host")
     return probs, lse, dscores, delta, d_sink
+
+
+def fos_qk_scores(q, k, scale: float = 1.0, scores=None, *, out_dtype=torch.float32,
+                  ld_scores=None, tile_n: int = 0, stream=None):
+    """Scores ``[B, Hq, Sq, Skv]`` = scale * Q K^T on the tensor cores (see ``fos_qk_scores``
+    in the C header).  ``q`` is ``[B, Hq, Sq, D]``, ``k`` ``[B, Hkv, Skv, D]``, both dense and of
+    one 16-bit dtype; ``scores`` (optional) is a ``[B, Hq, Sq, Skv]`` view whose rows are
+    ``ld_scores`` elements apart (a narrowed wider buffer).  When omitted it is allocated with
+    rows padded to 16 bytes (the tensor stores need it) and returned as the narrowed view."""
+    if q.dtype not in (torch.bfloat16, torch.float16) or k.dtype != q.dtype:
+        raise ValueError("q and k must share one dtype, bfloat16 or float16")
+    if q.dim() != 4 or k.dim() != 4 or not q.is_contiguous() or not k.is_contiguous():
+        raise ValueError("q and k must be dense [B, H, S, D] tensors")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Skv, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("q and k must agree in batch and head dimension")
+    dev = q.device
+    _check_cuda(k, "k", dev)
+    if scores is None:
+        per16 = 16 // torch.tensor([], dtype=out_dtype).element_size()
+        ld_pad = max(per16, -(-Skv // per16) * per16)
+        scores = torch.empty((B, Hq, Sq, ld_pad), dtype=out_dtype, device=dev)[..., :Skv]
+    if scores.dtype not in _DTYPES or tuple(scores.shape) != (B, Hq, Sq, Skv) or \
+            scores.stride(-1) != 1:
+        raise ValueError("scores must be [B, Hq, Sq, Skv] with unit key stride")
+    _check_cuda(scores, "scores", dev)
+    if scores.numel() == 0:  # no score to compute (strides of an empty tensor say nothing)
+        return scores
+    ld = scores.stride(2) if ld_scores is None else int(ld_scores)
+    if scores.stride(1) != Sq * ld or scores.stride(0) != Hq * Sq * ld:
+        raise ValueError("scores rows must be ld_scores apart and densely packed otherwise")
+    d = _abi.FosQkDesc(B, Hq, Hkv, Sq, Skv, D, ld, float(scale), int(tile_n))
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_qk_scores(ctypes.byref(d), _DTYPES[q.dtype], _DTYPES[scores.dtype],
+                                      _ptr(q), _ptr(k), _ptr(scores), _stream_handle(stream, dev))
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_qk_scores")
+    return scores
 
 
 def fos_device_error(stream=None, device=None) -> int:

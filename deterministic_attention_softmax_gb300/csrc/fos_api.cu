@@ -25,6 +25,11 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultWarps = 8;
 
 constexpr int kMaxStages = 16;
+// The group forward: at most 15 groups per CTA (one named barrier each), 128 ring barriers in
+// all, rings of at most 3 rows per group by default.
+constexpr int kMaxGroups = 15;
+constexpr int kGroupMaxBarriers = 128;
+constexpr int kGroupDefaultMaxStages = 3;
 
 struct DevInfo {
   bool ready = false;
@@ -105,6 +110,7 @@ fos_status check_launch(const fos_launch *l) {
   if (l->wait_timeout_ns < 0) return FOS_ERR_INVALID;
   if (l->test_stall != 0 && l->test_stall != 1) return FOS_ERR_INVALID;
   if (l->generic != 0 && l->generic != 1) return FOS_ERR_INVALID;
+  if (l->groups_per_cta < 0 || l->groups_per_cta > 15) return FOS_ERR_INVALID;
   return FOS_OK;
 }
 
@@ -413,6 +419,81 @@ fos_status run_fwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   return FOS_OK;
 }
 
+// The group forward (several row groups of `nw` warps per CTA, kt tiles parked per warp, no
+// producer warp): needs bulk copies (FOS_ERR_UNSUPPORTED otherwise, so the caller can fall back
+// to the CTA kernel with plain loads).  Groups per CTA and ring depth are chosen for the most
+// rows in flight per SM (registers, tensor-memory columns and shared memory all bound it), then
+// the deeper ring, then the smaller CTA.
+fos_status run_fwd_group(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
+                         const void *scores, void *probs, float *lse, cudaStream_t stream,
+                         const fos_launch *launch, const DevInfo &dev, int nw, int kt,
+                         bool fast) {
+  const int esz = dtype_size(dtype);
+  const int T = (desc->key_len + kTileK - 1) / kTileK;
+  const bool bulk_ok = aligned16(scores) && ((desc->ld * esz) & 15) == 0 &&
+                       (((int64_t)desc->key_len * esz) & 15) == 0;
+  if (!bulk_ok) return FOS_ERR_UNSUPPORTED;
+  fast = fast && ((desc->ld * esz) & 15) == 0 && aligned16(probs);
+  const size_t stage_bytes = (size_t)T * kTileK * esz;
+  cudaFuncAttributes fa;
+  if (fwd_group_attributes(dtype, kt, fast, &fa) != cudaSuccess) return FOS_ERR_CUDA;
+  const int max_g = 32 / nw < kMaxGroups ? 32 / nw : kMaxGroups;  // 1024 threads, 15 barriers
+  const int g_lo = (launch && launch->groups_per_cta) ? launch->groups_per_cta : 1;
+  const int g_hi = (launch && launch->groups_per_cta) ? launch->groups_per_cta : max_g;
+  const int s_lo = (launch && launch->stages) ? launch->stages : 1;
+  const int s_hi = (launch && launch->stages) ? launch->stages : kGroupDefaultMaxStages;
+  if (g_hi * nw > 32 || g_hi > kMaxGroups || g_lo * s_lo > kGroupMaxBarriers)
+    return FOS_ERR_UNSUPPORTED;
+  int best_g = 0, best_ns = 0, best_rows = 0, best_per = 0;
+  uint32_t best_cols = 0;
+  size_t best_smem = 0;
+  for (int ng = g_lo; ng <= g_hi; ++ng) {
+    const uint32_t cols = fwd_tmem_cols(ng * nw, kt);
+    if (cols > kTmemColsPerSm) continue;
+    for (int ns = s_lo; ns <= s_hi; ++ns) {
+      if (ng * ns > kGroupMaxBarriers) continue;
+      const size_t smem = fwd_group_smem(ng, ns, stage_bytes, T);
+      if (smem > (size_t)dev.max_smem) continue;
+      int per_sm = 0;
+      if (tmem_resident_ctas(dev, fa, ng * nw * 32, smem, cols, &per_sm) != cudaSuccess)
+        return FOS_ERR_CUDA;
+      const int rows = ng * per_sm;
+      // the most rows in flight; then the fewest CTAs per SM (more groups per CTA: measured
+      // 2-10 % faster at equal rows in flight on 17- to 32-tile rows); then the deeper ring
+      if (rows > best_rows || (rows == best_rows && per_sm < best_per) ||
+          (rows == best_rows && per_sm == best_per && ns > best_ns)) {
+        best_rows = rows;
+        best_g = ng;
+        best_ns = ns;
+        best_per = per_sm;
+        best_cols = cols;
+        best_smem = smem;
+      }
+    }
+  }
+  if (best_rows < 1) return FOS_ERR_UNSUPPORTED;
+  const int threads = best_g * nw * 32;
+  size_t smem = best_smem;
+  if (tmem_pad_smem(dev, fa, threads, best_cols, &smem) != cudaSuccess) return FOS_ERR_UNSUPPORTED;
+  int grid = (launch && launch->ctas) ? launch->ctas : best_per * dev.sms;
+  const int64_t need = (nrows + best_g - 1) / best_g;  // CTAs with at least one row
+  if ((int64_t)grid > need) grid = (int)need;
+
+  FwdArgs a{};
+  fill_rowwarp_args(desc, esz, row_base, nrows, T, best_ns, stage_bytes, probs, launch, dev, &a);
+  if (desc->sink) a.need_geo = 1;  // the merge needs the row's head
+  a.scores = scores;
+  a.probs = probs;
+  a.lse = lse;
+  a.sink = desc->sink;
+  a.keep_e = 1;
+  a.tmem_cols = best_cols;
+  a.group_warps = nw;
+  if (fwd_group_launch(dtype, kt, fast, a, grid, threads, smem, stream) != cudaSuccess)
+    return FOS_ERR_CUDA;
+  return FOS_OK;
+}
+
 fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
                    const void *scores, void *probs, float *lse, cudaStream_t stream,
                    const fos_launch *launch) {
@@ -468,6 +549,18 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
                     !desc->causal && !desc->kv_valid_len && !desc->key_mask && !desc->sink &&
                     aligned16(scores) && aligned16(probs) && ((desc->ld * esz) & 15) == 0 &&
                     (((int64_t)desc->key_len * esz) & 15) == 0;
+  // Every warp parks its tiles in tensor memory: the group kernel, unless the general CTA
+  // kernel or plain loads are asked for (or the rows do not allow bulk copies).  fp32 rows of
+  // 25..32 tiles keep their tuned CTA launch (measured faster there) unless groups are asked
+  // for.
+  const bool groups_asked = launch && launch->groups_per_cta;
+  if (in_regs && kt >= 4 && !(launch && (launch->generic || launch->load_path == 2)) &&
+      (!f32_mid || groups_asked)) {
+    st = run_fwd_group(desc, dtype, row_base, nrows, scores, probs, lse, stream, launch, *dev,
+                       warps, kt, fast);
+    if (st != FOS_ERR_UNSUPPORTED || (launch && launch->load_path == 1)) return st;
+  }
+  if (launch && launch->groups_per_cta) return FOS_ERR_UNSUPPORTED;  // only the group kernel
   // Parked e_j take tensor-memory columns; residency is then counted here (see
   // tmem_resident_ctas) and shared memory padded so that no SM takes more CTAs than it has
   // columns for.
@@ -499,11 +592,29 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   return FOS_OK;
 }
 
+// The sink gradient fused into the backward: octet layout of the problem's positions and the
+// arrays the kernels read (lse) and write (the octet sums).
+void fill_octets(const fos_desc *d, const float *lse, float *oct_sums, BwdArgs *a) {
+  a->lse = lse;
+  a->sink = d->sink;
+  a->oct_sums = oct_sums;
+  a->pos_end = (int64_t)d->batch * d->q_len;
+  a->oct_per_head = (a->pos_end + 7) / 8;
+  a->octdiv = make_fastdiv((uint32_t)(a->oct_per_head > 0 && a->oct_per_head < ((int64_t)1 << 32)
+                                          ? a->oct_per_head
+                                          : 1));
+  a->oct32 = ((int64_t)d->heads * a->oct_per_head < ((int64_t)1 << 32) &&
+              a->pos_end < ((int64_t)1 << 32))
+                 ? 1
+                 : 0;
+}
+
 // The one-warp-per-row backward for rows of at most kRowWarpMaxTiles tiles: needs bulk copies
 // of P and dP (FOS_ERR_UNSUPPORTED otherwise, so the caller can fall back to the CTA kernel).
 fos_status run_bwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
                            const void *probs, const void *dprobs, void *dscores, float *delta,
-                           cudaStream_t stream, const fos_launch *launch, const DevInfo &dev) {
+                           cudaStream_t stream, const fos_launch *launch, const DevInfo &dev,
+                           const float *lse = nullptr, float *oct_sums = nullptr) {
   const int esz = dtype_size(dtype);
   const int T = (desc->key_len + kTileK - 1) / kTileK;
   const bool bulk_ok = aligned16(probs) && aligned16(dprobs) && ((desc->ld * esz) & 15) == 0 &&
@@ -540,17 +651,21 @@ fos_status run_bwd_rowwarp(const fos_desc *desc, fos_dtype dtype, int64_t row_ba
   a.dprobs = dprobs;
   a.dscores = dscores;
   a.delta = delta;
-  if (bwd_rowwarp_launch(dtype, a, grid, threads, smem, stream) != cudaSuccess)
+  if (oct_sums) fill_octets(desc, lse, oct_sums, &a);
+  if (bwd_rowwarp_launch(dtype, a, grid, threads, smem, stream, oct_sums != nullptr) !=
+      cudaSuccess)
     return FOS_ERR_CUDA;
   return FOS_OK;
 }
 
 fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int64_t nrows,
                    const void *probs, const void *dprobs, void *dscores, float *delta,
-                   cudaStream_t stream, const fos_launch *launch) {
+                   cudaStream_t stream, const fos_launch *launch, const float *lse,
+                   float *oct_sums, bool *fused) {
   DevInfo *dev = nullptr;
   fos_status st = device_info(&dev);
   if (st != FOS_OK) return st;
+  if (fused) *fused = false;
 
   BwdArgs a{};
   Plan pl;
@@ -567,7 +682,8 @@ fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
     a.probs = probs;
     a.dprobs = dprobs;
     a.dscores = dscores;
-    a.delta = delta;
+    // no octets on this path: with a sink gradient to come, delta goes to the workspace
+    a.delta = (delta == nullptr && oct_sums) ? oct_sums : delta;
     if (bwd_stream_launch(dtype, a, pl.grid, pl.threads, pl.smem, stream) != cudaSuccess)
       return FOS_ERR_CUDA;
     return FOS_OK;
@@ -575,7 +691,8 @@ fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   if ((desc->key_len + kTileK - 1) / kTileK <= kRowWarpMaxTiles &&
       !(launch && (launch->generic || launch->load_path == 2))) {
     st = run_bwd_rowwarp(desc, dtype, row_base, nrows, probs, dprobs, dscores, delta, stream,
-                         launch, *dev);
+                         launch, *dev, lse, oct_sums);
+    if (st == FOS_OK && fused) *fused = oct_sums != nullptr;
     if (st != FOS_ERR_UNSUPPORTED || (launch && launch->load_path == 1)) return st;
     // unaligned rows: the CTA kernel with plain loads
   }
@@ -596,9 +713,21 @@ fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   a.dprobs = dprobs;
   a.dscores = dscores;
   a.delta = delta;
-  if (bwd_launch(dtype, fast && a.use_bulk && a.out_vec, a, pl.grid, pl.threads, pl.smem,
-                 stream) != cudaSuccess)
+  // The sink gradient rides along when there are enough octets to keep every CTA busy (each
+  // CTA then takes whole octets; with few of them the grid would idle).
+  bool fuse = false;
+  if (oct_sums) {
+    fill_octets(desc, lse, oct_sums, &a);
+    fuse = (int64_t)desc->heads * a.oct_per_head >= 4 * (int64_t)pl.grid;
+    if (!fuse) {  // delta then goes to the workspace for the sink-gradient kernel
+      a.oct_sums = nullptr;
+      if (delta == nullptr) a.delta = oct_sums;
+    }
+  }
+  if (bwd_launch(dtype, fast && a.use_bulk && a.out_vec, a, pl.grid, pl.threads, pl.smem, stream,
+                 fuse) != cudaSuccess)
     return FOS_ERR_CUDA;
+  if (fused) *fused = fuse;
   return FOS_OK;
 }
 
@@ -608,10 +737,7 @@ fos_status run_sink(const fos_desc *desc, const float *lse, const float *delta, 
   fos_status st = device_info(&dev);
   if (st != FOS_OK) return st;
   SinkArgs a{};
-  a.batch = desc->batch;
-  a.heads = desc->heads;
-  a.q_len = desc->q_len;
-  a.sink = desc->sink;
+  fill_sink_args(desc, &a);
   a.lse = lse;
   a.delta = delta;
   a.d_sink = d_sink;
@@ -644,6 +770,78 @@ extern "C" fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, con
   if (desc->rows == 0) return FOS_OK;  // nothing to do; empty buffers may be null
   if (probs == nullptr || dprobs == nullptr || dscores == nullptr) return FOS_ERR_INVALID;
   return run_bwd(desc, dtype, 0, desc->rows, probs, dprobs, dscores, delta, stream, launch);
+}
+
+extern "C" size_t fos_bwd_sink_workspace_bytes(const fos_desc *desc) {
+  if (check_desc(desc) != FOS_OK) return 0;
+  const int64_t octets = (int64_t)desc->heads * (((int64_t)desc->batch * desc->q_len + 7) / 8);
+  const int64_t n = desc->rows > octets ? desc->rows : octets;
+  return ((size_t)n * sizeof(float) + 255) & ~(size_t)255;
+}
+
+extern "C" fos_status fos_softmax_bwd_sink(const fos_desc *desc, fos_dtype dtype,
+                                           const void *probs, const void *dprobs, void *dscores,
+                                           float *delta, const float *lse, float *d_sink,
+                                           void *workspace, size_t workspace_bytes,
+                                           cudaStream_t stream, const fos_launch *launch) {
+  fos_status st = check_desc(desc);
+  if (st != FOS_OK) return st;
+  if ((st = check_launch(launch)) != FOS_OK) return st;
+  if (dtype_size(dtype) == 0) return FOS_ERR_INVALID;
+  if (desc->sink == nullptr || d_sink == nullptr) return FOS_ERR_INVALID;
+  if (desc->heads == 0) return FOS_OK;
+  const size_t need = fos_bwd_sink_workspace_bytes(desc);
+  if (desc->rows > 0 && (probs == nullptr || dprobs == nullptr || dscores == nullptr ||
+                         lse == nullptr || workspace == nullptr || workspace_bytes < need ||
+                         !aligned16(workspace)))
+    return FOS_ERR_INVALID;
+  float *ws = static_cast<float *>(workspace);
+  bool fused = false;
+  if (desc->rows > 0) {
+    // the workspace takes the octet sums, or delta (when none was given) if the rows go to a
+    // kernel that takes no octets; the sink-gradient kernel then follows (same bits)
+    st = run_bwd(desc, dtype, 0, desc->rows, probs, dprobs, dscores, delta, stream, launch, lse,
+                 ws, &fused);
+    if (st != FOS_OK) return st;
+  }
+  if (fused) {
+    DevInfo *dev = nullptr;
+    if ((st = device_info(&dev)) != FOS_OK) return st;
+    SinkArgs a{};
+    fill_sink_args(desc, &a);
+    a.d_sink = d_sink;
+    const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
+    if (sink_merge_launch(a, ws, ((int64_t)desc->batch * desc->q_len + 7) / 8, warps * 32,
+                          stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+    return FOS_OK;
+  }
+  return run_sink(desc, lse, delta ? delta : ws, d_sink, stream, launch);
+}
+
+extern "C" fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype,
+                                     fos_dtype out_dtype, const void *q, const void *k,
+                                     void *scores, cudaStream_t stream) {
+  if (desc == nullptr) return FOS_ERR_INVALID;
+  if (desc->tile_n != 0 && desc->tile_n != 128 && desc->tile_n != 256) return FOS_ERR_INVALID;
+  const fos_qk_desc &d = *desc;
+  if (d.batch < 0 || d.q_heads < 0 || d.kv_heads < 1 || d.q_len < 0 || d.kv_len < 0 ||
+      d.head_dim < 1 || d.ld_scores < d.kv_len || d.q_heads % d.kv_heads != 0)
+    return FOS_ERR_INVALID;
+  if (in_dtype != FOS_BF16 && in_dtype != FOS_F16) return FOS_ERR_INVALID;
+  if (out_dtype != FOS_F32 && out_dtype != FOS_BF16 && out_dtype != FOS_F16) return FOS_ERR_INVALID;
+  if ((int64_t)d.batch * d.q_heads * d.q_len * d.kv_len == 0) return FOS_OK;
+  if (q == nullptr || k == nullptr || scores == nullptr) return FOS_ERR_INVALID;
+  if (d.head_dim != 64 && d.head_dim != 128) return FOS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(scores) ||
+      ((d.ld_scores * dtype_size(out_dtype)) & 15) != 0)
+    return FOS_ERR_UNSUPPORTED;
+  if ((int64_t)d.batch * d.q_heads > 65535 || (d.q_len + 127) / 128 > 65535)
+    return FOS_ERR_UNSUPPORTED;
+  DevInfo *dev = nullptr;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
+  return run_qk(desc, in_dtype, out_dtype, q, k, scores, stream, dev->err, dev->max_smem);
 }
 
 extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
@@ -679,10 +877,7 @@ extern "C" fos_status fos_sink_grad_partials(const fos_desc *desc, int32_t batch
   DevInfo *dev = nullptr;
   if ((st = device_info(&dev)) != FOS_OK) return st;
   SinkArgs a{};
-  a.batch = desc->batch;
-  a.heads = desc->heads;
-  a.q_len = desc->q_len;
-  a.sink = desc->sink;
+  fill_sink_args(desc, &a);
   a.lse = lse;
   a.delta = delta;
   const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kDefaultWarps;
@@ -713,7 +908,7 @@ extern "C" fos_status fos_device_error(cudaStream_t stream) {
   if (v != 0) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return FOS_ERR_CUDA;
-    return FOS_ERR_TIMEOUT;
+    return v == 2u ? FOS_ERR_INDEX : FOS_ERR_TIMEOUT;  // 2: a debug-build index check
   }
   return FOS_OK;
 }
@@ -725,6 +920,7 @@ extern "C" const char *fos_status_string(fos_status status) {
     case FOS_ERR_UNSUPPORTED: return "FOS_ERR_UNSUPPORTED: valid but not supported by the kernels";
     case FOS_ERR_CUDA: return "FOS_ERR_CUDA: CUDA launch or runtime error";
     case FOS_ERR_TIMEOUT: return "FOS_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+    case FOS_ERR_INDEX: return "FOS_ERR_INDEX: an index check of the debug build failed";
   }
   return "unknown fos_status";
 }

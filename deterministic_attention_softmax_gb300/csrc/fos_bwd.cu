@@ -142,6 +142,80 @@ __device__ __forceinline__ void grad_tiles(const unsigned char *sp, const unsign
   }
 }
 
+// ---- the rows a CTA or a warp takes, in order
+//
+// Plain: rows first, first + step, ... below a.rows.  Octets (the sink gradient fused into
+// the backward): octets first, first + step, ... of all heads (octet o: head o / oct_per_head,
+// positions 8m .. 8m + 7 below pos_end, m = o % oct_per_head), each octet's rows in position
+// order, position p of head h being row (p / q_len * heads + h) * q_len + p % q_len.  The
+// cursor tells where an octet ends, so that its sum can be written.
+template <bool kOct>
+struct RowCursor;
+
+template <>
+struct RowCursor<false> {
+  int64_t r;
+  __device__ RowCursor(const BwdArgs &, int64_t first) : r(first) {}
+  __device__ bool valid(const BwdArgs &a) const { return r < a.rows; }
+  __device__ int64_t row() const { return r; }
+  __device__ void next(const BwdArgs &, int64_t step) { r += step; }
+};
+
+// The octet cursor moves from row to row incrementally: the next position of a head is the next
+// row (b, h, i + 1), or, past the last query of a batch entry, row (b + 1, h, 0), which lies
+// 1 + (heads - 1) * q_len rows further on.  Only a new octet needs divisions.
+template <>
+struct RowCursor<true> {
+  int64_t o;  // octet
+  int64_t r;  // current row
+  int32_t q;  // position within the octet
+  int32_t n;  // positions of this octet (8, fewer at the end of a head)
+  int32_t i;  // query index of the current row
+  int32_t h;  // head
+  __device__ RowCursor(const BwdArgs &a, int64_t first) : o(first) { seek(a); }
+  __device__ void seek(const BwdArgs &a) {
+    q = 0;
+    if (!valid(a)) return;
+    const int64_t hh = a.oct32 ? (int64_t)fast_div((uint32_t)o, a.octdiv) : o / a.oct_per_head;
+    const int64_t p = 8 * (o - hh * a.oct_per_head);
+    const int64_t b = a.oct32 ? (int64_t)fast_div((uint32_t)p, a.qdiv) : p / a.q_len;
+    h = (int32_t)hh;
+    i = (int32_t)(p - b * a.q_len);
+    n = (int32_t)min((int64_t)8, a.pos_end - p);
+    r = (b * a.heads + hh) * a.q_len + i;
+  }
+  __device__ bool valid(const BwdArgs &a) const { return o < (int64_t)a.heads * a.oct_per_head; }
+  __device__ int64_t row() const { return r; }
+  __device__ int64_t head() const { return h; }
+  __device__ bool octet_end() const { return q + 1 == n; }  // the current row is its octet's last
+  __device__ void next(const BwdArgs &a, int64_t step) {
+    if (octet_end()) {
+      o += step;
+      seek(a);
+    } else {
+      ++q;
+      if (++i == a.q_len) {
+        i = 0;
+        r += 1 + (int64_t)(a.heads - 1) * a.q_len;
+      } else {
+        ++r;
+      }
+    }
+  }
+};
+
+// Row r's term of the sink gradient, as the sink-gradient kernel forms it: c_r = -(exp(sink_h -
+// lse_r) * delta_r), with exp(sink_h - lse_r) taken as 0 for a -inf sink.  The sink and LSE
+// values are loaded when the row starts (sink_inputs), so their latency hides behind pass 1.
+__device__ __forceinline__ float2 sink_inputs(const BwdArgs &a, int64_t h, int64_t r) {
+  return make_float2(a.sink[h], a.lse[r]);
+}
+
+__device__ __forceinline__ float sink_term(float2 sl, float delta) {
+  const float ps = (sl.x == -INFINITY) ? 0.0f : scale_fos(sl.x, sl.y);
+  return -__fmul_rn(ps, delta);
+}
+
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
                                             int lim, bool vec, int nthreads) {
@@ -183,21 +257,21 @@ __device__ __forceinline__ void issue_row(const BwdArgs &a, int64_t rr, unsigned
 // Producer (lane 0 of the last warp): as in the forward, it alone issues the bulk copies
 // (P and dP of a row on one "full" barrier) once the compute warps have released the stage,
 // and waits for every copy it issued before it exits.
-template <typename T>
-__device__ void bwd_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
-                            uint64_t *full, uint64_t *empty, int4 *geos, unsigned char *ring,
-                            size_t slot, bool stall) {
+template <typename T, bool kOct>
+__device__ void bwd_produce(const BwdArgs &a, RowCursor<kOct> cur, int64_t step, uint64_t *full,
+                            uint64_t *empty, int4 *geos, unsigned char *ring, size_t slot,
+                            bool stall) {
   const int NS = a.stages;
   uint32_t issued = 0, last_ph = 0;
   int s = 0;
   uint32_t ph = 0;
-  for (int64_t kk = 0; kk < nmine; ++kk) {
+  for (int64_t kk = 0; cur.valid(a); ++kk, cur.next(a, step)) {
     if (kk >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, a.timeout_ns)) {
       raise_device_error(a.err, kDevErrTimeout);
       break;
     }
     const bool skip = stall && kk == 0;
-    issue_row<T>(a, r0 + kk * G, ring + (size_t)s * slot, &full[s], &geos[s], skip);
+    issue_row<T>(a, cur.row(), ring + (size_t)s * slot, &full[s], &geos[s], skip);
     if (!skip) {
       issued |= 1u << s;
       last_ph = (last_ph & ~(1u << s)) | (ph << s);
@@ -214,7 +288,7 @@ __device__ void bwd_produce(const BwdArgs &a, int64_t r0, int64_t G, int64_t nmi
 
 // kFast: the common case fixed at compile time (bulk copies, no mask, 16-byte aligned output).
 // Both instances do the same arithmetic in the same order.
-template <typename T, bool kFast>
+template <typename T, bool kFast, bool kSink>
 __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
@@ -232,9 +306,8 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
   const int w = tid >> 5;
   const int lane = tid & 31;
   const int64_t G = gridDim.x;
-  const int64_t r0 = blockIdx.x;
-  if (r0 >= a.rows) return;
-  const int64_t nmine = (a.rows - 1 - r0) / G + 1;
+  RowCursor<kSink> cur(a, blockIdx.x);
+  if (!cur.valid(a)) return;
   const int NS = a.stages;
   const bool use_bulk = kFast || a.use_bulk != 0;
 
@@ -250,18 +323,22 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
   }
   if (w == nw) {
     if (use_bulk && lane == 0)
-      bwd_produce<T>(a, r0, G, nmine, full, empty, geos, ring, slot,
-                     a.test_stall && blockIdx.x == 0);
+      bwd_produce<T, kSink>(a, cur, G, full, empty, geos, ring, slot,
+                            a.test_stall && blockIdx.x == 0);
     return;
   }
 
-  // stage index and phase parity of row k, carried rather than computed
+  // stage index and phase parity of the current row, carried rather than computed
   int s = 0;
   uint32_t ph = 0;
-  for (int64_t k = 0; k < nmine; ++k, s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
-    const int64_t r = r0 + k * G;
+  float acc = 0.0f;  // thread 0, sink fusion: the octet's ascending sum of c_r
+  for (; cur.valid(a); cur.next(a, G), s = (s + 1 == NS) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+    const int64_t r = cur.row();
     unsigned char *sp = ring + (size_t)s * slot;
     unsigned char *sd = sp + a.stage_bytes;
+    float2 sl = make_float2(0.0f, 0.0f);
+    if constexpr (kSink)
+      if (tid == 0) sl = sink_inputs(a, cur.head(), r);
 
     bool timed_out = false;
     int4 g;
@@ -280,8 +357,13 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
       compute_sync(ncomp);
     }
     const int lim = g.x;
-    const int Te = (lim + kTileK - 1) / kTileK;
+    int Te = (lim + kTileK - 1) / kTileK;
     const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+    if (!dbg_ok(a.err, Te <= a.T && (uint32_t)(Te * kTileK * esz) <= a.stage_bytes &&
+                           r < a.rows)) {
+      Te = 0;  // no tile is read, and the row stops below as after a wait that ran out
+      timed_out = true;
+    }
 
     // ---- pass 1: tile partials of delta, two tiles at a time
     delta_partials<T>(sp, sd, Te, w, nw, lane, lim, km, td);
@@ -303,6 +385,13 @@ __global__ void __maxnreg__(72) fos_bwd_kernel(const BwdArgs a) {
       for (; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
       dsm[0] = delta;
       if (a.delta) a.delta[r] = delta;
+      if constexpr (kSink) {
+        acc = __fadd_rn(acc, sink_term(sl, delta));
+        if (cur.octet_end()) {
+          a.oct_sums[cur.o] = acc;
+          acc = 0.0f;
+        }
+      }
     }
     compute_sync(ncomp);
     const float delta = dsm[0];
@@ -352,7 +441,7 @@ __device__ __forceinline__ void rw_issue(const BwdArgs &a, int64_t rr, unsigned 
   }
 }
 
-template <typename T>
+template <typename T, bool kSink>
 __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int esz = Io<T>::kEsz;
@@ -368,9 +457,8 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
   float *td = reinterpret_cast<float *>(smem + kBarBytes + kGeoBytes + (size_t)nw * NS * slot) +
               w * T4;
 
-  const int64_t GW = (int64_t)gridDim.x * nw;     // warps in the grid
-  const int64_t r0 = (int64_t)blockIdx.x * nw + w;  // this warp's first row
-  const int64_t nmine = r0 < a.rows ? (a.rows - 1 - r0) / GW + 1 : 0;
+  const int64_t GW = (int64_t)gridDim.x * nw;               // warps in the grid
+  RowCursor<kSink> cur(a, (int64_t)blockIdx.x * nw + w);      // the row being computed
   const bool stall = a.test_stall && blockIdx.x == 0 && w == 0;
 
   if (lane == 0) {
@@ -379,19 +467,24 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
   }
   __syncwarp();
   uint32_t issued = 0, last_ph = 0;
-  if (lane == 0)
-    for (int t = 0; t < NS && t < nmine; ++t)
-      if (!(stall && t == 0)) {  // test only: the very first copies are never issued
-        rw_issue<T>(a, r0 + t * GW, ring + (size_t)t * slot, &full[t], &geos[t]);
+  {
+    RowCursor<kSink> iss = cur;
+    for (int t = 0; t < NS && iss.valid(a); ++t, iss.next(a, GW))
+      if (lane == 0 && !(stall && t == 0)) {  // test only: the very first copies never issued
+        rw_issue<T>(a, iss.row(), ring + (size_t)t * slot, &full[t], &geos[t]);
         issued |= 1u << t;
       }
+  }
 
   int s = 0;
   uint32_t ph = 0;
   bool ok = true;
-  for (int64_t k = 0; k < nmine; ++k) {
-    const int64_t r = r0 + k * GW;
+  float acc = 0.0f;  // sink fusion: the octet's ascending sum of c_r (every lane the same)
+  for (; cur.valid(a); cur.next(a, GW)) {
+    const int64_t r = cur.row();
     unsigned char *sp = ring + (size_t)s * slot;
+    float2 sl = make_float2(0.0f, 0.0f);
+    if constexpr (kSink) sl = sink_inputs(a, cur.head(), r);
     // every lane waits; the warp stops as one if any lane's wait ran out
     const bool landed = mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
     if (!__all_sync(kFull, landed)) {
@@ -403,6 +496,11 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
     const int lim = g.x;
     const int Te = (lim + kTileK - 1) / kTileK;
     const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+    if (!dbg_ok(a.err, Te <= a.T && (uint32_t)(Te * kTileK * esz) <= a.stage_bytes &&
+                           r < a.rows)) {
+      ok = false;  // the warp stops as after a wait that ran out
+      break;
+    }
 
     // ---- pass 1: tile partials of delta, then their sum left to right (every lane)
     delta_partials<T>(sp, sp + a.stage_bytes, Te, 0, 1, lane, lim, km, td);
@@ -417,6 +515,13 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
       for (; t < Te; ++t) delta = __fadd_rn(delta, td[t]);
     }
     if (lane == 0 && a.delta) a.delta[r] = delta;
+    if constexpr (kSink) {
+      acc = __fadd_rn(acc, sink_term(sl, delta));
+      if (cur.octet_end()) {
+        if (lane == 0) a.oct_sums[cur.o] = acc;
+        acc = 0.0f;
+      }
+    }
 
     // ---- pass 2: dScores
     unsigned char *grow = static_cast<unsigned char *>(a.dscores) + (size_t)r * a.ld * esz;
@@ -429,10 +534,15 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
       store_lane8<T>(grow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
     }
     __syncwarp();  // td is rewritten by the next row; every lane is done with the buffer
-    if (lane == 0 && k + NS < nmine) {
-      rw_issue<T>(a, r + NS * GW, sp, &full[s], &geos[s]);
-      issued |= 1u << s;
-      last_ph = (last_ph & ~(1u << s)) | ((ph ^ 1u) << s);
+    {
+      // the row `stages` rows after this one goes into this buffer
+      RowCursor<kSink> iss = cur;
+      for (int t = 0; t < NS && iss.valid(a); ++t) iss.next(a, GW);
+      if (iss.valid(a) && lane == 0) {
+        rw_issue<T>(a, iss.row(), sp, &full[s], &geos[s]);
+        issued |= 1u << s;
+        last_ph = (last_ph & ~(1u << s)) | ((ph ^ 1u) << s);
+      }
     }
     if (++s == NS) {
       s = 0;
@@ -446,13 +556,19 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
         mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
 }
 
-const void *bwd_rowwarp_fn(fos_dtype dt) {
+template <bool kSink>
+const void *bwd_rowwarp_fn_s(fos_dtype dt) {
   switch (dt) {
-    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<float>);
-    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__nv_bfloat16>);
-    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__half>);
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<float, kSink>);
+    case FOS_BF16:
+      return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__nv_bfloat16, kSink>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_rowwarp_kernel<__half, kSink>);
   }
   return nullptr;
+}
+
+const void *bwd_rowwarp_fn(fos_dtype dt, bool sink = false) {
+  return sink ? bwd_rowwarp_fn_s<true>(dt) : bwd_rowwarp_fn_s<false>(dt);
 }
 
 // ------------------------------------------------ rows longer than shared memory (streaming)
@@ -651,17 +767,21 @@ const void *bwd_stream_fn(fos_dtype dt) {
   return nullptr;
 }
 
-template <bool kFast>
+template <bool kFast, bool kSink>
 const void *bwd_fn_f(fos_dtype dt) {
   switch (dt) {
-    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_kernel<float, kFast>);
-    case FOS_BF16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__nv_bfloat16, kFast>);
-    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__half, kFast>);
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_bwd_kernel<float, kFast, kSink>);
+    case FOS_BF16:
+      return reinterpret_cast<const void *>(&fos_bwd_kernel<__nv_bfloat16, kFast, kSink>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_bwd_kernel<__half, kFast, kSink>);
   }
   return nullptr;
 }
 
-const void *bwd_fn(fos_dtype dt, bool fast) { return fast ? bwd_fn_f<true>(dt) : bwd_fn_f<false>(dt); }
+const void *bwd_fn(fos_dtype dt, bool fast, bool sink = false) {
+  if (sink) return fast ? bwd_fn_f<true, true>(dt) : bwd_fn_f<false, true>(dt);
+  return fast ? bwd_fn_f<true, false>(dt) : bwd_fn_f<false, false>(dt);
+}
 
 }  // namespace
 
@@ -682,14 +802,16 @@ int bwd_default_warps(int T) {
 }
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem) {
-  for (bool fast : {false, true}) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_fn(dt, fast),
+  for (bool sink : {false, true}) {
+    for (bool fast : {false, true}) {
+      cudaError_t e = cudaFuncSetAttribute(bwd_fn(dt, fast, sink),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = cudaFuncSetAttribute(bwd_rowwarp_fn(dt, sink),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(bwd_rowwarp_fn(dt),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(bwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_smem);
 }
@@ -705,9 +827,9 @@ cudaError_t bwd_rowwarp_occupancy(fos_dtype dt, int threads, size_t smem, int *b
 }
 
 cudaError_t bwd_rowwarp_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool sink) {
   void *args[] = {const_cast<BwdArgs *>(&a)};
-  return cudaLaunchKernel(bwd_rowwarp_fn(dt), dim3(grid), dim3(threads), args, smem, s);
+  return cudaLaunchKernel(bwd_rowwarp_fn(dt, sink), dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm) {
@@ -727,9 +849,9 @@ cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int
 }
 
 cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
-                       size_t smem, cudaStream_t s) {
+                       size_t smem, cudaStream_t s, bool sink) {
   void *args[] = {const_cast<BwdArgs *>(&a)};
-  return cudaLaunchKernel(bwd_fn(dt, fast), dim3(grid), dim3(threads), args, smem, s);
+  return cudaLaunchKernel(bwd_fn(dt, fast, sink), dim3(grid), dim3(threads), args, smem, s);
 }
 
 }  // namespace fos

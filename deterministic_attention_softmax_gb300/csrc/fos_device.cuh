@@ -24,6 +24,7 @@ namespace fos {
 constexpr int kLaneKeys = 8;   // contiguous keys per lane inside a tile
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned kDevErrTimeout = 1u;  // value stored in the device error word
+constexpr unsigned kDevErrIndex = 2u;    // an index check of the debug build failed
 
 // ------------------------------------------------------------------ arithmetic contract
 
@@ -342,8 +343,41 @@ __device__ __forceinline__ bool compute_sync_or(int nthreads, bool flag) {
   return out != 0;
 }
 
+// The same two barriers with a barrier id of the caller's (1..15): one per group of warps
+// when a CTA holds several independent groups.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)flag), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
 __device__ __forceinline__ void raise_device_error(unsigned *err, unsigned code) {
   *reinterpret_cast<volatile unsigned *>(err) = code;
+}
+
+// Debug build (compiled with FOS_DEBUG): an index the caller is about to use lies outside its
+// array when `in_range` is false; that is recorded in the device error word and the caller skips
+// the access.  In the normal build this is `true` and compiles away.
+__device__ __forceinline__ bool dbg_ok(unsigned *err, bool in_range) {
+#ifdef FOS_DEBUG
+  if (!in_range) raise_device_error(err, kDevErrIndex);
+  return in_range;
+#else
+  (void)err;
+  (void)in_range;
+  return true;
+#endif
 }
 
 // ------------------------------------------------------------------ tensor memory (tcgen05)

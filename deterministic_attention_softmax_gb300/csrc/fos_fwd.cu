@@ -120,6 +120,72 @@ __device__ __forceinline__ void tile_stats2(const unsigned char *stage, int t0, 
   }
 }
 
+// The same pass 1 with the lane's key pointers given (p0, p1: keys 8 * lane of tiles t0, t1 in
+// the stage), so that a warp walking neighbouring tiles advances one pointer instead of
+// recomputing addresses; t0 / t1 still name the tiles for the masks and the statistics.
+template <typename T>
+__device__ __forceinline__ void lane_keys(const unsigned char *p, int t, int lane, int lim,
+                                          const uint8_t *km, float (&x)[8]) {
+  Io<T>::widen(Io<T>::lds(p), x);
+  if (km != nullptr || (t + 1) * kTileK > lim) mask_keys(x, t * kTileK + lane * kLaneKeys, lim, km);
+}
+
+template <typename T>
+__device__ __forceinline__ void tile_stats1p(const unsigned char *p0, int t0, int lane, int lim,
+                                             const uint8_t *km, float (&e)[8], float *tm,
+                                             float *ts) {
+  float x[8];
+  lane_keys<T>(p0, t0, lane, lim, km, x);
+  const float m = warp_max(max8(x));
+  float s = warp_sum_xor(tile_exp_sum(x, m, e));
+  if (lane == 0) {
+    tm[t0] = m;
+    ts[t0] = s;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void tile_stats2p(const unsigned char *p0, const unsigned char *p1,
+                                             int t0, int lane, int lim, const uint8_t *km,
+                                             float (&e0)[8], float (&e1)[8], float *tm,
+                                             float *ts) {
+  float x0[8], x1[8];
+  lane_keys<T>(p0, t0, lane, lim, km, x0);
+  lane_keys<T>(p1, t0 + 1, lane, lim, km, x1);
+  const float m0 = warp_max(max8(x0));
+  const float m1 = warp_max(max8(x1));
+  float s0 = tile_exp_sum(x0, m0, e0);
+  float s1 = tile_exp_sum(x1, m1, e1);
+  warp_sum_xor2(s0, s1);
+  if (lane == 0) {
+    tm[t0] = m0;
+    ts[t0] = s0;
+    tm[t0 + 1] = m1;
+    ts[t0 + 1] = s1;
+  }
+}
+
+// Pass 2's store of one tile at the lane's output pointer q (keys j0 .. j0 + 7 of the row).
+template <typename T>
+__device__ __forceinline__ void tile_store_p(unsigned char *q, int j0, int L, bool ovec,
+                                             const float (&e)[8], float c) {
+  float v[8];
+  const float2 cc = make_float2(c, c);
+#pragma unroll
+  for (int k = 0; k < kLaneKeys; k += 2) {  // packed: one rounding per component
+    const float2 pq = __fmul2_rn(make_float2(e[k], e[k + 1]), cc);
+    v[k] = pq.x;
+    v[k + 1] = pq.y;
+  }
+  if (ovec && j0 + kLaneKeys <= L) {
+    Io<T>::st8(q, v);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kLaneKeys; ++k)
+      if (j0 + k < L) Io<T>::st1(q + k * Io<T>::kEsz, v[k]);
+  }
+}
+
 // e_j of tile t again from the staged row and the stored tile maximum (same bits as pass 1).
 template <typename T>
 __device__ __forceinline__ void tile_exp(const unsigned char *stage, int t, int lane, int lim,
@@ -357,6 +423,9 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_kernel(const FwdArgs a) {
       for (int kk = 0; kk < KT; kk += 2) {
         const int t0 = w + kk * nw, t1 = t0 + nw;
         float e0[8], e1[8];
+        if (!dbg_ok(a.err, Te <= a.T && (uint32_t)(Te * kTileK * esz) <= a.stage_bytes &&
+                               (!park || ((tw - tbase) & 0xffffu) + kk * 8 + 16 <= a.tmem_cols)))
+          continue;
         if (t1 < Te) {
           tile_stats2<T>(stage, t0, t1, lane, lim, km, e0, e1, tm, ts);
           if constexpr (kRegs) {
@@ -417,6 +486,7 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_kernel(const FwdArgs a) {
     if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
     // ---- pass 2: P = e * c_t, one rounding, 16-byte stores
+    if (!dbg_ok(a.err, r < a.rows)) break;
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
     const bool ovec = kFast || a.out_vec != 0;
     if (keep) {
@@ -479,6 +549,210 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_kernel(const FwdArgs a) {
       tmem_fence_after();
       tmem_dealloc(tbase, a.tmem_cols);
     }
+  }
+}
+
+// Lane 0: the geometry of row rr into *geo and its bulk copy into `stage` on barrier `bar`.
+template <typename T>
+__device__ __forceinline__ void rw_issue(const FwdArgs &a, int64_t rr, unsigned char *stage,
+                                         uint64_t *bar, int4 *geo) {
+  constexpr int esz = Io<T>::kEsz;
+  const int4 g = row_geometry(a, rr);
+  *geo = g;
+  const uint32_t bytes = ((uint32_t)g.x * esz + 15u) & ~15u;  // never past the row
+  const uint32_t bar_a = smem_addr(bar);
+  fence_proxy_async_smem();  // the warp's reads of this buffer come before the copy
+  mbar_arrive_expect_tx(bar_a, bytes);
+  if (bytes)
+    bulk_g2s(smem_addr(stage),
+             static_cast<const unsigned char *>(a.scores) + (size_t)rr * a.ld * esz, bytes,
+             bar_a);
+}
+
+// ------------------------------------------------ several row groups per CTA
+//
+// The CTA kernel above gives every CTA a warp that only issues copies, and that warp's
+// registers count against the SM like a compute warp's.  Here a CTA holds `ng` groups of
+// `nw` compute warps and no producer warp.  Group gg = blockIdx.x * ng + g takes rows gg,
+// gg + gridDim.x * ng, ... one at a time, through its own ring of a.stages row buffers, and its
+// last warp issues its copies: the copy of row k + stages goes into row k's buffer right after
+// the group barrier that ends pass 1 of row k (the e_j are parked in tensor memory by then, so
+// the buffer is free), while the group's warp 0 merges.  Pass 1, the merge and pass 2 are the
+// CTA kernel's functions in the same order, so a row gives the same bits on either kernel.
+// Taken when every warp parks its tiles (4, 6 or 8 per warp) and rows come by bulk copy.
+
+constexpr int kGrpMaxBars = 128;  // "full" mbarriers (groups x stages) at the start
+constexpr int kGrpHead = kGrpMaxBars * 8 + kGrpMaxBars * 16;  // barriers, then row records
+
+template <typename T, int KT, bool kFast>
+__global__ void __maxnreg__(64) fos_fwd_group_kernel(const FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int esz = Io<T>::kEsz;
+  const int nw = a.group_warps;
+  const int ng = (blockDim.x >> 5) / nw;
+  const int NS = a.stages;
+  const int W = threadIdx.x >> 5;  // warp of the CTA: its tensor-memory lane quarter is W % 4
+  const int g = W / nw;
+  const int w = W - g * nw;  // warp of the group
+  const int lane = threadIdx.x & 31;
+  const int T4 = (a.T + 3) & ~3;
+  const int nstat = 2 * T4 + (T4 > 64 ? T4 : 64);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *full = bars + g * NS;
+  int4 *geos = reinterpret_cast<int4 *>(smem + kGrpMaxBars * 8) + g * NS;
+  unsigned char *ring = smem + kGrpHead + (size_t)g * NS * a.stage_bytes;
+  float *stats = reinterpret_cast<float *>(smem + kGrpHead + (size_t)ng * NS * a.stage_bytes);
+  float *tm = stats + g * nstat;
+  float *ts = tm + T4;
+  float *tc = ts + T4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stats + ng * nstat);
+
+  const int64_t GG = (int64_t)gridDim.x * ng;  // groups in the grid
+  const int64_t r0 = (int64_t)blockIdx.x * ng + g;
+  const int bar_id = 1 + g;  // named barrier of the group (ids 1..15)
+  const int gthreads = nw * 32;
+  const bool issuer = (w == nw - 1) && lane == 0;
+  const bool stall = a.test_stall && blockIdx.x == 0 && g == 0;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < ng * NS; ++t) mbar_init(smem_addr(&bars[t]), 1);
+    fence_mbar_init();
+  }
+  if (W == 0) tmem_alloc(smem_addr(tmem_slot), a.tmem_cols);
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // this warp's tile slots: lane quarter W % 4, KT * 8 columns from (W / 4) * KT * 8
+  const uint32_t tw = tbase + ((uint32_t)((W & 3) * 32) << 16) + (uint32_t)((W >> 2) * KT * 8);
+  constexpr int kPairUnroll = KT <= 6 ? 1 : KT / 2;
+
+  // prologue: the group's first rows (test only: the very first copy is never issued)
+  if (issuer)
+    for (int t = 0; t < NS && r0 + t * GG < a.rows; ++t)
+      if (!(stall && t == 0))
+        rw_issue<T>(a, r0 + t * GG, ring + (size_t)t * a.stage_bytes, &full[t], &geos[t]);
+
+  // Row j of the group always goes through stage j % NS, phase (j / NS) & 1, and the copies
+  // issued before row k's barrier are those of rows 0 .. k + NS - 1: after a timeout at row k
+  // the issuer knows which copies may still be in flight without keeping a record.
+  int s = 0;
+  uint32_t ph = 0;
+  int64_t r = r0;
+  bool ok = true;
+  for (; r < a.rows; r += GG) {
+    unsigned char *stage = ring + (size_t)s * a.stage_bytes;
+    const bool timed_out = !mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns);
+    // a copy that never landed leaves its record unwritten: no tile is then read
+    int4 gm = kFast ? make_int4(a.L, 0, 0, 0) : geos[s];
+    if (timed_out) gm.x = 0;
+    const int lim = gm.x;
+    const int Te = (lim + kTileK - 1) / kTileK;
+    const uint8_t *km = (!kFast && a.key_mask) ? a.key_mask + (int64_t)gm.y * a.L : nullptr;
+
+    // ---- pass 1: tile statistics, two neighbouring tiles at a time, e_j parked in tensor
+    // memory.  Warp w owns tiles tb .. tb + KT - 1 (any assignment gives the same bits); its
+    // lane pointer steps by two tiles.
+    const int tb = w * KT;
+    const int nt = Te - tb;  // tiles of this warp (at most KT; <= 0 when it has none)
+    {
+      const unsigned char *sp = stage + (size_t)(tb * kTileK + lane * kLaneKeys) * esz;
+#pragma unroll(kPairUnroll)
+      for (int kk = 0; kk < KT; kk += 2, sp += 2 * kTileK * esz) {
+        float e0[8], e1[8];
+        if (!dbg_ok(a.err, Te <= a.T && (uint32_t)(Te * kTileK * esz) <= a.stage_bytes &&
+                               ((tw - tbase) & 0xffffu) + kk * 8 + 16 <= a.tmem_cols &&
+                               r < a.rows))
+          continue;
+        if (kk + 1 < nt) {
+          tile_stats2p<T>(sp, sp + kTileK * esz, tb + kk, lane, lim, km, e0, e1, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+          tmem_st8(tw + kk * 8 + 8, e1);
+        } else if (kk < nt) {
+          tile_stats1p<T>(sp, tb + kk, lane, lim, km, e0, tm, ts);
+          __syncwarp();
+          tmem_st8(tw + kk * 8, e0);
+        }
+      }
+    }
+    if (named_sync_or(bar_id, gthreads, timed_out)) {
+      // A copy never landed: record it and stop (the issuer waits for its copies in flight;
+      // the tensor memory is freed below).
+      if (w == 0 && lane == 0) raise_device_error(a.err, kDevErrTimeout);
+      ok = false;
+      break;
+    }
+    // every warp of the group is done with the buffer: refill it with row r + stages
+    if (issuer && r + NS * GG < a.rows) rw_issue<T>(a, r + NS * GG, stage, &full[s], &geos[s]);
+
+    // ---- merge (warp 0 of the group)
+    float M = -INFINITY, S = 0.0f;
+    if (w == 0) {
+      if (!kFast && a.sink != nullptr) {
+        M = a.sink[gm.z];
+        S = 1.0f;
+      }
+      merge_tiles(Te, lane, tm, ts, tc, M, S);
+    }
+    named_sync(bar_id, gthreads);
+    if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
+
+    // ---- pass 2: P = e * c_t from the parked e_j, one rounding, 16-byte stores
+    unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
+    const bool ovec = kFast || a.out_vec != 0;
+    __syncwarp();
+    tmem_wait_st();  // this warp's pass-1 values have landed
+    {
+      const int j0 = tb * kTileK + lane * kLaneKeys;  // the lane's first key
+      unsigned char *pp = prow + (size_t)j0 * esz;
+#pragma unroll(kPairUnroll)
+      for (int kk = 0; kk < KT; kk += 2, pp += 2 * kTileK * esz) {
+        float e0[8], e1[8];
+        if (!dbg_ok(a.err, ((tw - tbase) & 0xffffu) + kk * 8 + 16 <= a.tmem_cols && r < a.rows))
+          continue;
+        const int jk = j0 + kk * kTileK;
+        if (kk + 1 < nt) {
+          tmem_ld16(tw + kk * 8, e0, e1);
+          const float2 c = *reinterpret_cast<const float2 *>(tc + tb + kk);
+          tile_store_p<T>(pp, jk, a.L, ovec, e0, c.x);
+          tile_store_p<T>(pp + kTileK * esz, jk + kTileK, a.L, ovec, e1, c.y);
+        } else if (kk < nt) {
+          tmem_ld8(tw + kk * 8, e0);
+          tile_store_p<T>(pp, jk, a.L, ovec, e0, tc[tb + kk]);
+        }
+      }
+    }
+    // tiles past the row's last candidate key: P = +0 (this warp's tiles below T)
+    for (int t = (Te > tb ? Te : tb); t < tb + KT && t < a.T; ++t) {
+      float z[8];
+#pragma unroll
+      for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
+      store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
+    }
+    // Tile t's tm / ts entries are written by its warp in pass 1 and read by warp 0's merge
+    // between the group's two barriers; tc is rewritten after the next row's first barrier.
+    if (++s == NS) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  // after a timeout at row k, every copy the issuer started (rows k .. k + NS - 1; row 0 not
+  // in the test's stall) lands before the CTA can exit
+  if (!ok && issuer) {
+    const int64_t k = (r - r0) / GG;
+    for (int64_t j = k; j < k + NS && r0 + j * GG < a.rows; ++j)
+      if (!(stall && j == 0))
+        mbar_wait_bounded(smem_addr(&full[j % NS]), (uint32_t)(j / NS) & 1u, a.timeout_ns);
+  }
+  // every warp is done with its columns: free them
+  __syncwarp();
+  tmem_wait_st();
+  tmem_fence_before();
+  __syncthreads();
+  if (W == 0) {
+    tmem_fence_after();
+    tmem_dealloc(tbase, a.tmem_cols);
   }
 }
 
@@ -609,7 +883,9 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
       const int t0 = seg * SEG, nt = min(SEG, Te - t0);
       const int lim_l = lim - t0 * kTileK;  // the segment's keys are numbered from 0
       const uint8_t *kms = km ? km + t0 * kTileK : nullptr;
-      int tl = w;
+      if (!dbg_ok(a.err, Te <= a.T && (nt <= 0 || (uint32_t)(nt * kTileK * esz) <= a.stage_bytes)))
+        timed_out = true;  // stop the row as a failed wait would
+      int tl = timed_out ? nt : w;
       for (; tl + nw < nt; tl += 2 * nw) {
         float e0[8], e1[8];
         tile_stats2<T>(stage, tl, tl + nw, lane, lim_l, kms, e0, e1, tm + t0, ts + t0);
@@ -702,23 +978,6 @@ const void *fwd_stream_fn(fos_dtype dt) {
 // the buffer of row k as soon as pass 1 of row k has read it.  The per-tile arithmetic, the
 // merge and pass 2 are those of fos_fwd_kernel, so a row gives the same bits on either kernel.
 
-// Lane 0: the geometry of row rr into *geo and its bulk copy into `stage` on barrier `bar`.
-template <typename T>
-__device__ __forceinline__ void rw_issue(const FwdArgs &a, int64_t rr, unsigned char *stage,
-                                         uint64_t *bar, int4 *geo) {
-  constexpr int esz = Io<T>::kEsz;
-  const int4 g = row_geometry(a, rr);
-  *geo = g;
-  const uint32_t bytes = ((uint32_t)g.x * esz + 15u) & ~15u;  // never past the row
-  const uint32_t bar_a = smem_addr(bar);
-  fence_proxy_async_smem();  // the warp's reads of this buffer come before the copy
-  mbar_arrive_expect_tx(bar_a, bytes);
-  if (bytes)
-    bulk_g2s(smem_addr(stage),
-             static_cast<const unsigned char *>(a.scores) + (size_t)rr * a.ld * esz, bytes,
-             bar_a);
-}
-
 template <typename T, int KT>
 __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -787,6 +1046,12 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
     const int lim = g.x;
     const int Te = (lim + kTileK - 1) / kTileK;
     const uint8_t *km = a.key_mask ? a.key_mask + (int64_t)g.y * a.L : nullptr;
+    if (!dbg_ok(a.err, Te <= KT && (uint32_t)(Te * kTileK * esz) <= a.stage_bytes &&
+                           r < a.rows &&
+                           (kRegs || ((tw - *tmem_slot) & 0xffffu) + KT * 8 <= a.tmem_cols))) {
+      ok = false;
+      break;
+    }
 
     // ---- pass 1: every tile of the row, two neighbouring tiles at a time
     float er0[8], er1[8];  // kRegs: the row's pair, kept for pass 2
@@ -885,6 +1150,27 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
   }
 }
 
+template <int KT, bool kFast>
+const void *fwd_group_fn_kt(fos_dtype dt) {
+  switch (dt) {
+    case FOS_F32: return reinterpret_cast<const void *>(&fos_fwd_group_kernel<float, KT, kFast>);
+    case FOS_BF16:
+      return reinterpret_cast<const void *>(&fos_fwd_group_kernel<__nv_bfloat16, KT, kFast>);
+    case FOS_F16: return reinterpret_cast<const void *>(&fos_fwd_group_kernel<__half, KT, kFast>);
+  }
+  return nullptr;
+}
+
+template <bool kFast>
+const void *fwd_group_fn_f(fos_dtype dt, int kt) {
+  return kt <= 4 ? fwd_group_fn_kt<4, kFast>(dt)
+                 : (kt <= 6 ? fwd_group_fn_kt<6, kFast>(dt) : fwd_group_fn_kt<8, kFast>(dt));
+}
+
+const void *fwd_group_fn(fos_dtype dt, int kt, bool fast) {
+  return fast ? fwd_group_fn_f<true>(dt, kt) : fwd_group_fn_f<false>(dt, kt);
+}
+
 template <int KT>
 const void *fwd_rowwarp_fn_kt(fos_dtype dt) {
   switch (dt) {
@@ -975,6 +1261,16 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
                                (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
     }
+  for (int kt : {4, 6, 8})
+    for (bool fast : {false, true}) {
+      cudaError_t e = cudaFuncSetAttribute(fwd_group_fn(dt, kt, fast),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fwd_group_fn(dt, kt, fast),
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
   for (int kt : {2, 4, 8}) {
     cudaError_t e = cudaFuncSetAttribute(fwd_rowwarp_fn(dt, kt),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
@@ -985,6 +1281,24 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem) {
   }
   return cudaFuncSetAttribute(fwd_stream_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               max_smem);
+}
+
+size_t fwd_group_smem(int groups, int stages, size_t stage_bytes, int T) {
+  // barriers and row records, the groups' rings, their statistics, the tensor-memory address
+  const int T4 = (T + 3) & ~3;
+  const size_t nstat = (size_t)(2 * T4 + (T4 > 64 ? T4 : 64));
+  return (size_t)kGrpHead + (size_t)groups * stages * stage_bytes +
+         (size_t)groups * nstat * sizeof(float) + 16;
+}
+
+cudaError_t fwd_group_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa) {
+  return cudaFuncGetAttributes(fa, fwd_group_fn(dt, kt, fast));
+}
+
+cudaError_t fwd_group_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid,
+                             int threads, size_t smem, cudaStream_t s) {
+  void *args[] = {const_cast<FwdArgs *>(&a)};
+  return cudaLaunchKernel(fwd_group_fn(dt, kt, fast), dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t fwd_rowwarp_launch(fos_dtype dt, int kt, const FwdArgs &a, int grid, int threads,

@@ -75,6 +75,7 @@ struct FwdArgs : RowArgs {
                        // KT tiles); otherwise they are recomputed in the second pass
   uint32_t tmem_cols;  // tensor-memory columns a CTA allocates to keep them in; 0 when none
                        // (two tiles per warp stay in registers)
+  int32_t group_warps; // group kernel: compute warps per row group (blockDim / 32 / groups)
 };
 
 // Tensor-memory columns per SM, and the columns a forward CTA of `warps` compute warps with
@@ -87,6 +88,17 @@ struct BwdArgs : RowArgs {
   const void *dprobs;
   void *dscores;
   float *delta;  // [rows] or null
+  // The sink gradient fused into the backward: rows are taken by octets, 8 consecutive
+  // positions (b, i) of one head (octet o: head o / oct_per_head, positions 8m .. 8m + 7 with
+  // m = o % oct_per_head, those below pos_end), and each octet's ascending float32 sum of
+  // c_r = -(exp(sink_h - lse_r) * delta_r) is written to oct_sums[o].
+  const float *lse;       // [rows]
+  const float *sink;      // [heads]
+  float *oct_sums;        // [heads * oct_per_head]
+  int64_t oct_per_head;   // ceil(batch * q_len / 8)
+  int64_t pos_end;        // batch * q_len
+  FastDiv octdiv;         // division by oct_per_head
+  int32_t oct32;          // octet indices and positions fit 32 bits
 };
 
 struct SinkArgs {
@@ -95,7 +107,19 @@ struct SinkArgs {
   const float *lse;
   const float *delta;
   float *d_sink;
+  FastDiv qdiv;   // division by q_len
+  int32_t pos32;  // batch * q_len < 2^32: positions divide in 32 bits
 };
+
+// The fields of SinkArgs every sink launch shares.
+inline void fill_sink_args(const fos_desc *d, SinkArgs *a) {
+  a->batch = d->batch;
+  a->heads = d->heads;
+  a->q_len = d->q_len;
+  a->sink = d->sink;
+  a->qdiv = make_fastdiv((uint32_t)d->q_len);
+  a->pos32 = ((int64_t)d->batch * d->q_len < ((int64_t)1 << 32)) ? 1 : 0;
+}
 
 // Shared memory used by a row kernel besides its ring of staged rows.
 size_t fwd_extra_smem(int T, int stages);
@@ -116,6 +140,12 @@ cudaError_t fwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t fwd_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa);
 cudaError_t fwd_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid, int threads,
                        size_t smem, cudaStream_t s);
+// Several row groups per CTA (each `a.group_warps` warps, one row at a time, its own ring of
+// a.stages buffers, no producer warp); kt = 4, 6 or 8 tiles per warp parked in tensor memory.
+size_t fwd_group_smem(int groups, int stages, size_t stage_bytes, int T);
+cudaError_t fwd_group_attributes(fos_dtype dt, int kt, bool fast, cudaFuncAttributes *fa);
+cudaError_t fwd_group_launch(fos_dtype dt, int kt, bool fast, const FwdArgs &a, int grid,
+                             int threads, size_t smem, cudaStream_t s);
 // Rows of at most 8 tiles, one warp per row: kt = 2, 4 or 8 tiles parked in a.tmem_cols
 // tensor-memory columns; `warps` warps per CTA, each with a.stages row buffers of
 // a.stage_bytes.
@@ -130,21 +160,32 @@ cudaError_t fwd_stream_launch(fos_dtype dt, const FwdArgs &a, int grid, int thre
 
 cudaError_t bwd_prepare(fos_dtype dt, int max_smem);
 cudaError_t bwd_occupancy(fos_dtype dt, bool fast, int threads, size_t smem, int *blocks_per_sm);
+// `sink`: the instance that takes rows by octets and writes their sink-gradient sums.
 cudaError_t bwd_launch(fos_dtype dt, bool fast, const BwdArgs &a, int grid, int threads,
-                       size_t smem, cudaStream_t s);
+                       size_t smem, cudaStream_t s, bool sink = false);
 // Short rows, one warp per row (P and dP of a row per buffer; T4 floats of partials per warp).
 size_t bwd_rowwarp_smem(int warps, int stages, size_t stage_bytes, int T);
 cudaError_t bwd_rowwarp_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t bwd_rowwarp_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
-                               cudaStream_t s);
+                               cudaStream_t s, bool sink = false);
 cudaError_t bwd_stream_occupancy(fos_dtype dt, int threads, size_t smem, int *blocks_per_sm);
 cudaError_t bwd_stream_launch(fos_dtype dt, const BwdArgs &a, int grid, int threads, size_t smem,
                               cudaStream_t s);
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s);
+// d_sink from the octet sums the fused backward wrote (the chunk tree and left-to-right sum of
+// sink_launch on them).
+cudaError_t sink_merge_launch(const SinkArgs &a, const float *oct_sums, int64_t oct_per_head,
+                              int threads, cudaStream_t s);
 // Chunk partials of the batch entries [b0, b1) (arrays hold their rows from b0 * heads * q_len).
 cudaError_t sink_partials_launch(const SinkArgs &a, int64_t b0, int64_t b1, float *partials,
                                  int threads, cudaStream_t s);
+
+// The QK contraction (fos_qk.cu): dynamic shared memory of a CTA, and the launch on validated
+// arguments (err: the device error word).
+size_t qk_smem_bytes(int head_dim, int tile_n);
+fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *q,
+                  const void *k, void *scores, cudaStream_t stream, unsigned *err, int max_smem);
 
 // Host-side checks shared by the C ABI entry points (fos_api.cu).
 int dtype_size(fos_dtype dt);
@@ -157,9 +198,14 @@ fos_status check_launch(const fos_launch *l);
 fos_status run_fwd(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
                    const void *scores, void *probs, float *lse, cudaStream_t s,
                    const fos_launch *l);
+// With oct_sums (and lse) given, the backward may also take the sink gradient's octet sums
+// (rows taken by octets; whole problem only, row_base 0); *fused tells whether it did.  When
+// it did not and delta is null, delta is written to oct_sums instead (which must then hold
+// nrows floats).
 fos_status run_bwd(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t nrows,
                    const void *probs, const void *dprobs, void *dscores, float *delta,
-                   cudaStream_t s, const fos_launch *l);
+                   cudaStream_t s, const fos_launch *l, const float *lse = nullptr,
+                   float *oct_sums = nullptr, bool *fused = nullptr);
 fos_status run_sink(const fos_desc *d, const float *lse, const float *delta, float *d_sink,
                     cudaStream_t s, const fos_launch *l);
 

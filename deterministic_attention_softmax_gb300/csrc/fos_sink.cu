@@ -31,7 +31,13 @@ __device__ __forceinline__ float sink_chunk(const SinkArgs &a, int h, float sk, 
   for (int q = 0; q < kLaneKeys; ++q) {
     const int64_t p = c * kTileK + lane * kLaneKeys + q;
     if (p < pos_end) {
-      const int64_t r = ((p / a.q_len) * a.heads + h) * a.q_len + (p % a.q_len) - row_base;
+      int64_t b;
+      if (a.pos32) {
+        b = fast_div((uint32_t)p, a.qdiv);
+      } else {
+        b = p / a.q_len;
+      }
+      const int64_t r = (b * a.heads + h) * a.q_len + (p - b * a.q_len) - row_base;
       const float ps = (sk == -INFINITY) ? 0.0f : scale_fos(sk, a.lse[r]);
       acc = __fadd_rn(acc, -__fmul_rn(ps, a.delta[r]));
     }
@@ -85,7 +91,45 @@ __global__ void __launch_bounds__(1024) fos_sink_kernel(const SinkArgs a) {
   if (tid == 0) a.d_sink[h] = total;
 }
 
+// d_sink from the octet sums the backward wrote when it took the sink gradient along: lane l
+// of chunk c holds octet 32c + l's sum (+0 past the head's last octet), which is that lane's
+// ascending sum in sink_chunk, so the tree and the left-to-right chunk sum below give the bits
+// of fos_sink_kernel.
+__global__ void __launch_bounds__(1024) fos_sink_merge_kernel(const SinkArgs a,
+                                                              const float *oct_sums,
+                                                              int64_t oct_per_head) {
+  __shared__ float part[32];
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nw = blockDim.x >> 5;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t nchunks = (oct_per_head + 31) / 32;
+  const float *os = oct_sums + (int64_t)h * oct_per_head;
+  float total = 0.0f;
+  for (int64_t base = 0; base < nchunks; base += nw) {
+    const int64_t c = base + w;
+    if (c < nchunks) {
+      const int64_t m = c * 32 + lane;
+      const float acc = warp_sum_xor(m < oct_per_head ? os[m] : 0.0f);
+      if (lane == 0) part[w] = acc;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int q = 0; q < nw && base + q < nchunks; ++q) total = __fadd_rn(total, part[q]);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) a.d_sink[h] = total;
+}
+
 }  // namespace
+
+cudaError_t sink_merge_launch(const SinkArgs &a, const float *oct_sums, int64_t oct_per_head,
+                              int threads, cudaStream_t s) {
+  fos_sink_merge_kernel<<<a.heads, threads, 0, s>>>(a, oct_sums, oct_per_head);
+  return cudaGetLastError();
+}
 
 cudaError_t sink_launch(const SinkArgs &a, int threads, cudaStream_t s) {
   fos_sink_kernel<<<a.heads, threads, 0, s>>>(a);

@@ -67,6 +67,10 @@
  *   FOS_ERR_CUDA         the launch failed (cudaGetLastError after the launch).
  *   FOS_ERR_TIMEOUT      reported by fos_device_error(): a bounded wait inside a kernel ran
  *                        out, the kernel stopped early and its outputs are not valid.
+ *   FOS_ERR_INDEX        reported by fos_device_error() of the debug build only (the library
+ *                        compiled with FOS_DEBUG, whose kernels check their stage offsets,
+ *                        tensor-memory columns and row indices before using them): a check
+ *                        failed and the access was skipped.
  * rows == 0 is valid and launches nothing (the array pointers may then be NULL).
  */
 #ifndef FOS_SOFTMAX_H
@@ -93,7 +97,9 @@ typedef enum fos_status {
   FOS_ERR_INVALID = 1,
   FOS_ERR_UNSUPPORTED = 2,
   FOS_ERR_CUDA = 3,
-  FOS_ERR_TIMEOUT = 4
+  FOS_ERR_TIMEOUT = 4,
+  FOS_ERR_INDEX = 5 /* debug build only (compiled with FOS_DEBUG): an index check in a kernel
+                       failed, the access was skipped and the outputs are not valid */
 } fos_status;
 
 /* Problem description shared by the three operations. */
@@ -125,8 +131,14 @@ typedef struct fos_launch {
   int64_t wait_timeout_ns; /* 0 = default (2 s): limit of every bounded wait in a kernel */
   int32_t test_stall;    /* 0; 1 = CTA 0 waits on a copy that is never issued (test only) */
   int32_t generic;       /* 0 = auto; 1 = the general one-CTA-per-row kernels only: neither the
-                            instances specialised for unmasked rows nor the one-warp-per-row
-                            kernels for rows of at most 8 tiles (same bits) */
+                            instances specialised for unmasked rows, nor the forward's row
+                            groups, nor the one-warp-per-row kernels for rows of at most 8
+                            tiles (same bits) */
+  int32_t groups_per_cta; /* 0 = default; forward rows whose warps keep all their tiles'
+                            exponentials (4, 6 or 8 tiles per warp, bulk copies): row groups of
+                            warps_per_cta warps per CTA, 1..15, each with its own ring of
+                            `stages` rows; FOS_ERR_UNSUPPORTED where that kernel does not apply
+                            (same bits) */
 } fos_launch;
 
 /*
@@ -176,6 +188,36 @@ fos_status fos_softmax_bwd(const fos_desc *desc, fos_dtype dtype, const void *pr
  */
 fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,
                          float *d_sink, cudaStream_t stream, const fos_launch *launch);
+
+/*
+ * The backward and the sink gradient in one call: the results of fos_softmax_bwd followed by
+ * fos_sink_grad, bit for bit.  Where the backward's kernels allow it (rows of at most 8 tiles,
+ * and longer staged rows with at least four octets per CTA), they take the rows by octets, 8
+ * consecutive positions (b, i) of one head, and write each octet's ascending float32 sum of
+ * c_r = -(exp(sink_h - lse_r) * delta_r) to the workspace; a small kernel then combines them
+ * per head by the sink gradient's own chunk tree and left-to-right order, so delta and LSE are
+ * never read back and no atomic is used.  Otherwise (rows streamed in segments) the two
+ * launches run.  ("[ROCm] Jax Add softmax sink (learnable off-by-one) support", Description and
+ * review thread: d_sink reduced per head inside the backward; there by atomicAdd into a zeroed
+ * buffer, here in a fixed order.)
+ *   desc->sink    required (FOS_ERR_INVALID otherwise)
+ *   probs, dprobs, dscores, delta  as fos_softmax_bwd (delta may be NULL)
+ *   lse           device float [rows] (input, as written by the forward)
+ *   d_sink        device float [heads] (output)
+ *   workspace     device, 16-byte aligned, at least fos_bwd_sink_workspace_bytes(desc) bytes
+ *                 (the octet sums, or delta when none is given and the rows are streamed);
+ *                 owned by the caller, not to be touched until `stream` completes
+ * heads == 0 is a no-op; rows == 0 writes d_sink = 0.
+ */
+fos_status fos_softmax_bwd_sink(const fos_desc *desc, fos_dtype dtype, const void *probs,
+                                const void *dprobs, void *dscores, float *delta,
+                                const float *lse, float *d_sink, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream,
+                                const fos_launch *launch);
+
+/* Workspace bytes of fos_softmax_bwd_sink: 4 * max(rows, heads * ceil(batch * q_len / 8)),
+ * rounded up to 256 (0 for an invalid description).  Host arithmetic only. */
+size_t fos_bwd_sink_workspace_bytes(const fos_desc *desc);
 
 /*
  * The sink gradient with the rows sharded by batch entry (one shard per device, say): each
@@ -281,9 +323,49 @@ fos_status fos_softmax_step_host_static(const fos_desc *desc, fos_dtype dtype,
                                         const fos_launch *launch);
 
 /*
+ * The QK contraction in front of the softmax: scores[b, h, i, j] = scale * sum_d q[b, h, i, d]
+ * * k[b, h / (q_heads / kv_heads), j, d] on the tensor cores, the head dimension accumulated in
+ * float32 in a fixed order (steps of 16, ascending), then multiplied by `scale` (one rounding)
+ * and rounded once to the output dtype.  Each score depends only on its query row and key row,
+ * so it has the same bits whatever the batch, the heads around it or its position.
+ * ("Batch-invariant attention (standard softmax--cuda version)", Fixed Reduction Contract: one
+ * writer per score, the head dimension in a fixed order; "[WS1][kernels] Add fixed-order
+ * joint-attention softmax for Qwen-Image", Summary: the QK GEMM feeds the softmax.)
+ */
+typedef struct fos_qk_desc {
+  int32_t batch;      /* B */
+  int32_t q_heads;    /* Hq, a multiple of kv_heads */
+  int32_t kv_heads;   /* Hkv >= 1; query head h reads key head h / (Hq / Hkv) */
+  int32_t q_len;      /* Sq, query rows per (batch, query head) */
+  int32_t kv_len;     /* Skv, keys per (batch, key head) */
+  int32_t head_dim;   /* D: 64 or 128 */
+  int64_t ld_scores;  /* elements between rows of scores, >= kv_len */
+  float scale;        /* applied to the float32 sum (e.g. 1 / sqrt(D)) */
+  int32_t tile_n;     /* keys per CTA tile: 0 = default, 128 or 256 (no result bit depends on
+                         it; each score's sum is the same sequence of instructions) */
+} fos_qk_desc;
+
+/*
+ *   q       device [batch][q_heads][q_len][head_dim] of in_dtype (FOS_BF16 or FOS_F16), dense
+ *   k       device [batch][kv_heads][kv_len][head_dim] of in_dtype, dense
+ *   scores  device [batch][q_heads][q_len][ld_scores] of out_dtype (FOS_F32, FOS_BF16 or
+ *           FOS_F16); columns kv_len .. ld_scores-1 are not written
+ * q, k and scores must start on 16-byte boundaries and ld_scores * (size of out_dtype) must be
+ * a multiple of 16 (FOS_ERR_UNSUPPORTED otherwise); scores must not overlap q or k.
+ * FOS_ERR_INVALID for a bad description (negative sizes, q_heads not a multiple of kv_heads,
+ * ld_scores < kv_len, tile_n not 0, 128 or 256) or dtype; FOS_ERR_UNSUPPORTED for another head dimension
+ * or more than 65535 (batch x query heads) or query tiles of 128.  A problem with no score is a
+ * no-op.  Resources: each CTA allocates tile_n (128 by default) tensor-memory columns and frees
+ * them before it exits.  A bounded wait that runs out is reported by fos_device_error() as FOS_ERR_TIMEOUT.
+ */
+fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
+                         const void *q, const void *k, void *scores, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device error word of the current
- * device: FOS_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call, FOS_OK
- * otherwise (FOS_ERR_CUDA if the synchronisation itself failed).
+ * device: FOS_ERR_TIMEOUT if a kernel's bounded wait ran out since the last call, FOS_ERR_INDEX
+ * if an index check of the debug build failed, FOS_OK otherwise (FOS_ERR_CUDA if the
+ * synchronisation itself failed).
  */
 fos_status fos_device_error(cudaStream_t stream);
 

@@ -14,6 +14,10 @@ The bounds are the stated correctness bar of the kernels, read as follows:
   float32 sum's rounding errors are relative to its partial sums, whose size is set by the
   absolute terms, so no fixed-order float32 sum reaches 2^-20 * |delta| when delta cancels.
 * delta (float32): |err| <= 1e-5 * sum_k P_k |dP_k|.
+* QK scores: |err| <= 2^-16 * |scale| * sum_d |q_d k_d| (a float32 sum of the head dimension's
+  products, whatever its order, stays within (D - 1) * 2^-24 of that absolute sum, 2^-17 at
+  D = 128; 2^-16 leaves room for the final multiply by the scale), plus one ULP of the FP64 value
+  for a 16-bit output dtype (its single rounding).
 * d_sink (float32): |err| <= 1e-5 * sum_r |c_r| with c_r = exp(sink_h - LSE_r) * delta_r.
 """
 
@@ -110,6 +114,18 @@ def check_dsink(gpu, ref, lse, delta, sink, batch, heads, q_len):
     with np.errstate(invalid="ignore", over="ignore"):
         c = np.where(np.isneginf(sk), 0.0, np.exp(sk - lse) * delta)
     bound = 1e-5 * np.abs(c).sum(axis=(0, 2)) + 1e-30
+    err = np.abs(gpu - ref)
+    w, i = _worst(err, bound)
+    return bool(np.all(err <= bound)), w, i
+
+
+def check_scores(gpu, ref, abs_dot, scale, dtype: str):
+    """QK scores; abs_dot = sum_d |q_d k_d| per score (float64, same shape as ref)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = 2.0 ** -16 * abs(float(scale)) * np.asarray(abs_dot, dtype=np.float64) + 1e-30
+    if dtype != "float32":
+        bound = bound + ulp(ref, dtype)
     err = np.abs(gpu - ref)
     w, i = _worst(err, bound)
     return bool(np.all(err <= bound)), w, i

@@ -249,3 +249,37 @@ def test_more_ctas_than_tensor_memory_serves(L, opts):
     torch.cuda.synchronize()
     assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1])
     assert fos.fos_device_error() == 0
+
+
+# ------------------------------------------------------------------ row groups per CTA
+
+
+@pytest.mark.parametrize("dtype_name", ["bfloat16", "float32", "float16"])
+@pytest.mark.parametrize("L", [2304, 4352, 8192, 16384])
+@pytest.mark.parametrize("masked", [False, True], ids=["unmasked", "masked"])
+def test_row_groups_per_cta_give_the_same_bits(dtype_name, L, masked):
+    # Rows whose warps park all their tiles in tensor memory run as row groups, several per
+    # CTA, each group with its own ring of row buffers and its last warp issuing the copies.
+    # Every split (groups per CTA, ring depth, CTAs) gives the bits of the general
+    # one-row-per-CTA kernel; a split that does not fit the SM is refused as unsupported.
+    dt = DTYPES[dtype_name]
+    if masked:
+        x, _, kw = masked_case(dt, L=L, Sq=48)
+    else:
+        x, kw = W.normal((700, L), 4.0, 51, dt, dev()), {}
+    ref = fos.fos_softmax_fwd(x, launch=fos.Launch(generic=1), **kw)
+    ran = 0
+    for ng in (1, 2, 3, 4, 5, 8, 10):
+        for ns in (1, 2, 3):
+            for ctas in (0, 7):
+                try:
+                    out = fos.fos_softmax_fwd(
+                        x, launch=fos.Launch(groups_per_cta=ng, stages=ns, ctas=ctas), **kw)
+                except fos.FosError as e:
+                    assert e.status == 2, (ng, ns, ctas)  # FOS_ERR_UNSUPPORTED
+                    continue
+                assert bits_equal(ref[0], out[0]) and bits_equal(ref[1], out[1]), (ng, ns, ctas)
+                ran += 1
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+    assert ran >= 6

@@ -188,3 +188,18 @@ def test_a_zero_reference_allows_only_the_smallest_spacing(dtype, spacing):
     p = np.zeros((1, 2))  # P = 0 on the key: the float32 floor is 0 as well
     dp = np.ones((1, 2))
     assert not tol.check_dscores(np.array([[2 * spacing, 0.0]]), ref, p, dp, dtype)[0]
+
+
+
+@pytest.mark.parametrize("dtype,one", [("float32", 0.0), ("bfloat16", 2.0 ** -7),
+                                       ("float16", 2.0 ** -10)])
+def test_check_scores_bound(dtype, one):
+    # score 1.5 with scale 0.5 and sum_d |q_d k_d| = 8: floor 2^-16 * 0.5 * 8 = 2^-14, plus one
+    # ULP at 1.5 for a 16-bit output (2^-7 bf16, 2^-10 fp16)
+    ref = np.array([1.5])
+    absd = np.array([8.0])
+    bound = 2.0 ** -14 + one
+    assert tol.check_scores(ref + 0.99 * bound, ref, absd, 0.5, dtype)[0]
+    assert not tol.check_scores(ref - 1.01 * bound, ref, absd, 0.5, dtype)[0]
+    # the scale's sign does not matter
+    assert tol.check_scores(ref + 0.99 * bound, ref, absd, -0.5, dtype)[0]
