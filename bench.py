@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
     ap.add_argument("--workload-iters", type=int, default=20)
-    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "pv"],
+                    default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
     return ap.parse_args()
@@ -543,7 +544,7 @@ def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
         odt_c = {torch.float32: _abi.FOS_F32, torch.bfloat16: _abi.FOS_BF16}[odt]
         sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
         qp, kp, sp_ = (ctypes.c_void_p(t.data_ptr()) for t in (q, k, s))
-        for tile_n in (0, 256):  # the default (128 keys per tile), then 256
+        for tile_n in (0, 128, 256):  # the default (persistent), then one CTA per tile
             d = _abi.FosQkDesc(B, H, H, Sq, Skv, D, s.stride(2), scale, tile_n)
             dr = ctypes.byref(d)
             evs = []
@@ -568,12 +569,55 @@ def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
                   tflops_peak}
             if tile_n == 0:
                 res.update(r_)
-                res["tile_n"] = 128
+                res["kernel"] = "persistent: one CTA per SM over 128 x 128 tiles"
             else:
-                res["tile_n_256"] = r_
+                res[f"one_cta_per_tile_n_{tile_n}"] = r_
         out[name] = res
         del s
-    del q, k, scratch
+    # ---- PV on the same shape: the benchmark's P (probability-shaped, bf16) times V (D = 128)
+    g2 = torch.Generator(device=dev).manual_seed(62)
+    pm = (torch.rand(B, H, Sq, Skv, generator=g2, device=dev).pow(4) * (5.0 / Skv)).to(
+        torch.bfloat16)
+    vv = torch.randn(B, H, Skv, D, generator=g2, device=dev).to(torch.bfloat16)
+    pv = {"flops_per_launch": 2.0 * B * H * Sq * Skv * D}
+    o = fos.fos_pv_out(pm, vv)
+    rows = np.unique(np.concatenate([[0, Sq - 1], np.random.default_rng(2).integers(0, Sq, 24)]))
+    r = torch.from_numpy(rows).to(dev)
+    pn, vn = pm[:, :, r].double().cpu().numpy(), vv.double().cpu().numpy()
+    ok, worst, _ = tol.check_pv(o[:, :, r].double().cpu().numpy(), gemm.pv(pn, vn),
+                                gemm.pv(np.abs(pn), np.abs(vn)), "float32")
+    if not ok:
+        raise SystemExit(f"PV parity gate failed: worst {worst}")
+    from deterministic_attention_softmax_gb300 import _abi
+
+    lib = _abi.lib()
+    d = _abi.FosPvDesc(B, H, H, Sq, Skv, D, pm.stride(2))
+    sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    args = (ctypes.byref(d), _abi.FOS_BF16, _abi.FOS_F32, ctypes.c_void_p(pm.data_ptr()),
+            ctypes.c_void_p(vv.data_ptr()), ctypes.c_void_p(o.data_ptr()), sh)
+    evs = []
+    for it in range(warmup + iters):
+        scratch.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if lib.fos_pv_out(*args) != _abi.FOS_OK:
+            raise SystemExit("fos_pv_out failed while timing")
+        e1.record()
+        if it >= warmup:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    if fos.fos_device_error() != 0:
+        raise SystemExit("device error while timing the PV contraction")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    nbytes = pm.numel() * 2 + vv.numel() * 2 + o.numel() * 4
+    pv.update({"cold_ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+               "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+               "tflops": pv["flops_per_launch"] / (ms * 1e-3) / 1e12,
+               "frac_of_bf16_tensor": pv["flops_per_launch"] / (ms * 1e-3) / 1e12 / tflops_peak,
+               "algorithmic_bytes": nbytes, "out": "float32",
+               "parity_gate": {"rows": int(len(rows)), "worst_err_over_bound": worst}})
+    out["pv_out"] = pv
+    del q, k, scratch, pm, vv, o
     torch.cuda.empty_cache()
     return out
 
@@ -829,6 +873,16 @@ def run_profile(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fos.build()
+    if args.profile == "pv":  # the PV contraction on the Qwen-Image shape (float32 outputs)
+        g = torch.Generator(device=dev).manual_seed(62)
+        pm = torch.rand(1, 4, 4096, 4352, generator=g, device=dev).to(torch.bfloat16)
+        vv = torch.randn(1, 4, 4352, 128, generator=g, device=dev).to(torch.bfloat16)
+        o = fos.fos_pv_out(pm, vv)
+        for _ in range(args.warmup + args.steps):
+            fos.fos_pv_out(pm, vv, o)
+        torch.cuda.synchronize()
+        assert fos.fos_device_error() == 0
+        return
     if args.profile == "qk":  # the QK contraction on the Qwen-Image shape (float32 scores)
         g = torch.Generator(device=dev).manual_seed(61)
         q = torch.randn(1, 4, 4096, 128, generator=g, device=dev).to(torch.bfloat16)

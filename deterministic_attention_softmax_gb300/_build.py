@@ -18,8 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfos_softmax.so")
-SOURCES = ["fos_api.cu", "fos_fwd.cu", "fos_bwd.cu", "fos_sink.cu", "fos_host.cu", "fos_qk.cu"]
+SOURCES = ["fos_api.cu", "fos_fwd.cu", "fos_bwd.cu", "fos_sink.cu", "fos_host.cu", "fos_qk.cu",
+           "fos_pv.cu"]
 HEADERS = [os.path.join(CSRC, "fos_device.cuh"), os.path.join(CSRC, "fos_internal.h"),
+           os.path.join(CSRC, "fos_tc.cuh"),
            os.path.join(ROOT, "include", "fos_softmax.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

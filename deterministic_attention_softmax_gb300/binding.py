@@ -436,6 +436,40 @@ def fos_qk_scores(q, k, scale: float = 1.0, scores=None, *, out_dtype=torch.floa
     return scores
 
 
+def fos_pv_out(probs, v, out=None, *, out_dtype=torch.float32, stream=None):
+    """Output ``[B, Hq, Sq, D]`` = P V on the tensor cores (see ``fos_pv_out`` in the C header).
+    ``probs`` is a ``[B, Hq, Sq, Skv]`` view whose rows are ``ld`` elements apart (``ld`` a
+    multiple of 8), ``v`` a dense ``[B, Hkv, Skv, D]`` of the same 16-bit dtype."""
+    if probs.dtype not in (torch.bfloat16, torch.float16) or v.dtype != probs.dtype:
+        raise ValueError("probs and v must share one dtype, bfloat16 or float16")
+    if probs.dim() != 4 or v.dim() != 4 or not v.is_contiguous() or probs.stride(-1) != 1:
+        raise ValueError("probs must be [B, H, Sq, Skv] with unit key stride, v dense "
+                         "[B, Hkv, Skv, D]")
+    B, Hq, Sq, Skv = probs.shape
+    Bv, Hkv, Skv_v, D = v.shape
+    if Bv != B or Skv_v != Skv:
+        raise ValueError("probs and v must agree in batch and key count")
+    dev = probs.device
+    _check_cuda(v, "v", dev)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=dev)
+    if out.dtype not in _DTYPES or tuple(out.shape) != (B, Hq, Sq, D) or not out.is_contiguous():
+        raise ValueError("out must be a dense [B, Hq, Sq, D] tensor")
+    _check_cuda(out, "out", dev)
+    if out.numel() == 0:
+        return out
+    ld = probs.stride(2)
+    if probs.stride(1) != Sq * ld or probs.stride(0) != Hq * Sq * ld:
+        raise ValueError("probs rows must be one stride apart and densely packed otherwise")
+    d = _abi.FosPvDesc(B, Hq, Hkv, Sq, Skv, D, ld)
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_pv_out(ctypes.byref(d), _DTYPES[probs.dtype], _DTYPES[out.dtype],
+                                   _ptr(probs), _ptr(v), _ptr(out), _stream_handle(stream, dev))
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_pv_out")
+    return out
+
+
 def fos_device_error(stream=None, device=None) -> int:
     """Synchronise the stream and return (and clear) the device error status code."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device

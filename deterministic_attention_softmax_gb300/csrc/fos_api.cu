@@ -841,7 +841,30 @@ extern "C" fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype,
   DevInfo *dev = nullptr;
   fos_status st = device_info(&dev);
   if (st != FOS_OK) return st;
-  return run_qk(desc, in_dtype, out_dtype, q, k, scores, stream, dev->err, dev->max_smem);
+  return run_qk(desc, in_dtype, out_dtype, q, k, scores, stream, dev->err, dev->max_smem,
+                dev->sms);
+}
+
+extern "C" fos_status fos_pv_out(const fos_pv_desc *desc, fos_dtype in_dtype,
+                                  fos_dtype out_dtype, const void *probs, const void *v,
+                                  void *out, cudaStream_t stream) {
+  if (desc == nullptr) return FOS_ERR_INVALID;
+  const fos_pv_desc &d = *desc;
+  if (d.batch < 0 || d.q_heads < 0 || d.kv_heads < 1 || d.q_len < 0 || d.kv_len < 1 ||
+      d.head_dim < 1 || d.ld_probs < d.kv_len || d.q_heads % d.kv_heads != 0)
+    return FOS_ERR_INVALID;
+  if (in_dtype != FOS_BF16 && in_dtype != FOS_F16) return FOS_ERR_INVALID;
+  if (out_dtype != FOS_F32 && out_dtype != FOS_BF16 && out_dtype != FOS_F16) return FOS_ERR_INVALID;
+  if ((int64_t)d.batch * d.q_heads * d.q_len == 0) return FOS_OK;
+  if (probs == nullptr || v == nullptr || out == nullptr) return FOS_ERR_INVALID;
+  if (d.head_dim != 64 && d.head_dim != 128) return FOS_ERR_UNSUPPORTED;
+  if (!aligned16(probs) || !aligned16(v) || !aligned16(out) || (d.ld_probs & 7) != 0)
+    return FOS_ERR_UNSUPPORTED;
+  if ((int64_t)d.batch * d.q_heads > 65535) return FOS_ERR_UNSUPPORTED;
+  DevInfo *dev = nullptr;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
+  return run_pv(desc, in_dtype, out_dtype, probs, v, out, stream, dev->err, dev->max_smem);
 }
 
 extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,

@@ -480,7 +480,9 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
   uint32_t ph = 0;
   bool ok = true;
   float acc = 0.0f;  // sink fusion: the octet's ascending sum of c_r (every lane the same)
-  for (; cur.valid(a); cur.next(a, GW)) {
+  while (cur.valid(a)) {
+    RowCursor<kSink> nxt = cur;  // the warp's next row, for the copy and for the next iteration
+    nxt.next(a, GW);
     const int64_t r = cur.row();
     unsigned char *sp = ring + (size_t)s * slot;
     float2 sl = make_float2(0.0f, 0.0f);
@@ -536,14 +538,15 @@ __global__ void __maxnreg__(72) fos_bwd_rowwarp_kernel(const BwdArgs a) {
     __syncwarp();  // td is rewritten by the next row; every lane is done with the buffer
     {
       // the row `stages` rows after this one goes into this buffer
-      RowCursor<kSink> iss = cur;
-      for (int t = 0; t < NS && iss.valid(a); ++t) iss.next(a, GW);
+      RowCursor<kSink> iss = nxt;
+      for (int t = 1; t < NS && iss.valid(a); ++t) iss.next(a, GW);
       if (iss.valid(a) && lane == 0) {
         rw_issue<T>(a, iss.row(), sp, &full[s], &geos[s]);
         issued |= 1u << s;
         last_ph = (last_ph & ~(1u << s)) | ((ph ^ 1u) << s);
       }
     }
+    cur = nxt;
     if (++s == NS) {
       s = 0;
       ph ^= 1u;

@@ -185,7 +185,13 @@ cudaError_t sink_partials_launch(const SinkArgs &a, int64_t b0, int64_t b1, floa
 // arguments (err: the device error word).
 size_t qk_smem_bytes(int head_dim, int tile_n);
 fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *q,
-                  const void *k, void *scores, cudaStream_t stream, unsigned *err, int max_smem);
+                  const void *k, void *scores, cudaStream_t stream, unsigned *err, int max_smem,
+                  int sms);
+
+// The PV contraction (fos_pv.cu), as the QK one.
+size_t pv_smem_bytes(int head_dim);
+fos_status run_pv(const fos_pv_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *p,
+                  const void *v, void *out, cudaStream_t stream, unsigned *err, int max_smem);
 
 // Host-side checks shared by the C ABI entry points (fos_api.cu).
 int dtype_size(fos_dtype dt);

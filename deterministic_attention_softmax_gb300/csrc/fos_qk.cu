@@ -29,6 +29,7 @@
 
 #include "fos_device.cuh"
 #include "fos_internal.h"
+#include "fos_tc.cuh"
 
 namespace fos {
 namespace {
@@ -37,10 +38,9 @@ constexpr int kBM = 128;   // query rows per tile (MMA M, TMEM lanes)
 constexpr int kKB = 64;    // head-dimension elements per 128-byte swizzle block
 constexpr int kUK = 16;    // head-dimension elements per MMA
 constexpr int kQkThreads = 128;
-constexpr int kQkDefaultTileN = 128;
-// Keys per tile by default: 128 lets three CTAs share an SM (about 65 KB of shared memory and
-// 128 tensor-memory columns each), so more CTAs drain their scores while others load and
-// multiply; 256 takes two.
+// A CTA per tile (tile_n 128 or 256 keys): 128 lets three CTAs share an SM (about 65 KB of
+// shared memory and 128 tensor-memory columns each), 256 two.  The default is the persistent
+// form below.
 
 // Shared-memory layout (dynamic; 1024-byte aligned operand blocks), BN keys per tile (128 or
 // 256, the MMA's N and the accumulator's columns):
@@ -49,93 +49,6 @@ constexpr int kQkDefaultTileN = 128;
 // After the MMAs, the operand region holds the epilogue's staging: 4 warps x 2 buffers x 4 KB.
 constexpr int kABlock = kBM * kKB * 2;
 constexpr int kStage = 32 * 128;  // 32 rows x 128 bytes
-
-// ---- tcgen05 operand descriptors (PTX ISA, "Matrix Descriptors" of the tcgen05 family)
-//
-// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle layout: rows of
-// 128 bytes (64 bf16 of the head dimension), 8-row swizzle atoms of 1024 bytes, atoms
-// 1024 bytes apart (stride byte offset); bits 0-13 start address >> 4, 16-29 leading byte
-// offset >> 4 (unused by this layout, set to 1), 32-45 stride byte offset >> 4, 46-48 the
-// fixed value 0b001, 49-51 base offset (0: every block starts 1024-byte aligned), 61-63 the
-// layout (2 = 128-byte swizzle).  A step of 16 elements along K inside the 128-byte row
-// advances the start address by 32 bytes.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: float32 accumulator (bits 4-5 = 1), A and B of the
-// same 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t qk_idesc(bool bf16, int bn) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(dtmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every MMA this thread issued has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                          int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store3(const CUtensorMap *map, int x, int y, int z,
-                                           uint32_t src) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most `n` (0 or 1) of this thread's bulk store groups still read shared memory.
-__device__ __forceinline__ void bulk_wait_read(int n) {
-  if (n == 0)
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  else
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
-// Warp-wide: each lane reads 32 consecutive columns of its own lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t ta, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(ta)
-      : "memory");
-#pragma unroll
-  for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]);
-}
 
 struct QkArgs {
   int32_t dblocks;    // head dimension / 64 (1 or 2)
@@ -258,41 +171,171 @@ __global__ void __launch_bounds__(kQkThreads, 1)
   }
 }
 
-// ---- host: tensor maps through the driver's entry point (no link against libcuda)
+// ---- persistent form: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... of
+// 128 x 128 scores (key tile fastest).  Warp 0 issues the copies into two operand stages, warp 1
+// the MMAs into two accumulators (2 x 128 tensor-memory columns), warps 2..9 drain an
+// accumulator (two warps per lane quarter, 64 columns each) while the next tile's copies and
+// MMAs proceed.  Each tile's scores are the same instructions on the same operands as in
+// fos_qk_kernel, so the bits are the same.
+constexpr int kPqBN = 128;
+constexpr int kPqThreads = 320;
+constexpr int kPqEpiWarps = 8;
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+struct QkTiles {
+  int32_t nx, ny;  // key tiles, query tiles per (batch, head)
+  int64_t ntiles;  // nx * ny * batch * q_heads
+};
 
-EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  });
-  return fn;
-}
+template <typename OutT>
+__global__ void __launch_bounds__(kPqThreads, 1)
+    fos_qk_persistent_kernel(const __grid_constant__ CUtensorMap qmap,
+                             const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap smap, const QkArgs a,
+                             const QkTiles tl, uint32_t idesc) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  constexpr int kBBlock = kPqBN * kKB * 2;  // 16 KB
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int stage_bytes = a.dblocks * (kABlock + kBBlock);
+  unsigned char *staging = smem + 2 * stage_bytes;  // 8 warps x 2 x 4 KB
+  uint64_t *bars = reinterpret_cast<uint64_t *>(staging + kPqEpiWarps * 2 * kStage);
+  uint64_t *full = bars, *empty = bars + 2, *accf = bars + 4, *acce = bars + 6;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-// A 3-D map over [heads][rows][cols] elements, rows `row_bytes` apart, heads `head_bytes`
-// apart, with a box of box_cols x box_rows x 1 and the 128-byte swizzle.
-bool make_map3(CUtensorMap *m, CUtensorMapDataType ty, const void *base, uint64_t cols,
-               uint64_t rows, uint64_t heads, uint64_t row_bytes, uint64_t head_bytes,
-               uint32_t box_cols, uint32_t box_rows) {
-  EncodeTiled enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {cols, rows, heads};
-  const cuuint64_t strides[2] = {row_bytes, head_bytes};
-  const cuuint32_t box[3] = {box_cols, box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, ty, 3, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), 1);
+      mbar_init(smem_addr(&accf[i]), 1);
+      mbar_init(smem_addr(&acce[i]), kPqEpiWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 2 * kPqBN);
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tacc = *tmem_slot;
+  const int64_t per_z = (int64_t)tl.nx * tl.ny;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- copies
+      int64_t i = 0;
+      for (int64_t t = blockIdx.x; t < tl.ntiles; t += gridDim.x, ++i) {
+        const int s = (int)(i & 1);
+        if (i >= 2 && !mbar_wait_bounded(smem_addr(&empty[s]), (uint32_t)((i >> 1) & 1) ^ 1u,
+                                         a.timeout_ns)) {
+          raise_device_error(a.err, kDevErrTimeout);
+          break;
+        }
+        const int zq = (int)(t / per_z);
+        const int rem = (int)(t - (int64_t)zq * per_z);
+        const int y = rem / tl.nx, x = rem - y * tl.nx;
+        const int zk = (zq / a.q_heads) * (a.q_heads / a.group) + (zq % a.q_heads) / a.group;
+        unsigned char *sa = smem + s * stage_bytes;
+        unsigned char *sb = sa + a.dblocks * kABlock;
+        const uint32_t fb = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+        for (int kb = 0; kb < a.dblocks; ++kb) {
+          tma_load3(smem_addr(sa + kb * kABlock), &qmap, kb * kKB, y * kBM, zq, fb);
+          tma_load3(smem_addr(sb + kb * kBBlock), &kmap, kb * kKB, x * kPqBN, zk, fb);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMAs: tile i into accumulator i % 2, head dimension ascending
+      int64_t i = 0;
+      for (int64_t t = blockIdx.x; t < tl.ntiles; t += gridDim.x, ++i) {
+        const int s = (int)(i & 1);
+        if (!mbar_wait_bounded(smem_addr(&full[s]), (uint32_t)((i >> 1) & 1), a.timeout_ns) ||
+            (i >= 2 && !mbar_wait_bounded(smem_addr(&acce[s]), (uint32_t)((i >> 1) & 1) ^ 1u,
+                                          a.timeout_ns))) {
+          raise_device_error(a.err, kDevErrTimeout);
+          break;
+        }
+        tmem_fence_after();
+        unsigned char *sa = smem + s * stage_bytes;
+        unsigned char *sb = sa + a.dblocks * kABlock;
+        const uint32_t dacc = tacc + (uint32_t)(s * kPqBN);
+        for (int kb = 0; kb < a.dblocks; ++kb)
+          for (int k = 0; k < kKB / kUK; ++k) {
+            const uint64_t ad = sw128_desc(smem_addr(sa + kb * kABlock + k * kUK * 2));
+            const uint64_t bd = sw128_desc(smem_addr(sb + kb * kBBlock + k * kUK * 2));
+            mma_f16(dacc, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+        mma_commit(smem_addr(&empty[s]));  // the stage may be refilled
+        mma_commit(smem_addr(&accf[s]));   // the accumulator may be drained
+      }
+    }
+  } else {
+    // ---- epilogue: warp w drains lane quarter w % 4, columns 64 * ((w - 2) / 4) .. + 63
+    constexpr int kCols = 128 / (int)sizeof(OutT);  // 32 float or 64 bf16 / fp16 columns
+    const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
+    unsigned char *stage0 = staging + ew * 2 * kStage;
+    int nst = 0;  // stores issued by this warp
+    int64_t i = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < tl.ntiles && ok; t += gridDim.x, ++i) {
+      const int b = (int)(i & 1);
+      ok = __all_sync(kFull, mbar_wait_bounded(smem_addr(&accf[b]), (uint32_t)((i >> 1) & 1),
+                                               a.timeout_ns));
+      if (!ok) {
+        if (lane == 0) raise_device_error(a.err, kDevErrTimeout);
+        break;
+      }
+      tmem_fence_after();
+      const int zq = (int)(t / per_z);
+      const int rem = (int)(t - (int64_t)zq * per_z);
+      const int y = rem / tl.nx, x = rem - y * tl.nx;
+      const uint32_t trow = tacc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kPqBN + half * 64);
+      for (int c = 0; c < 64 / kCols; ++c, ++nst) {
+        unsigned char *st = stage0 + (nst & 1) * kStage;
+        if (lane == 0 && nst >= 2) bulk_wait_read(1);
+        __syncwarp();
+        uint32_t packed[32];
+#pragma unroll
+        for (int h = 0; h < kCols / 32; ++h) {
+          float v[32];
+          tmem_ld32(trow + (uint32_t)(c * kCols + h * 32), v);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __fmul_rn(v[q], a.scale);
+          if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) packed[q] = __float_as_uint(v[q]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; q += 2)
+              packed[h * 16 + q / 2] = Io<OutT>::pack(v[q], v[q + 1]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 *dst = reinterpret_cast<uint4 *>(st + lane * 128 + ((j ^ (lane & 7)) << 4));
+          *dst = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                            packed[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store3(&smap, x * kPqBN + half * 64 + c * kCols, y * kBM + quarter * 32, zq,
+                     smem_addr(st));
+          bulk_commit();
+        }
+      }
+      // this warp is done reading the accumulator: the MMAs of tile i + 2 may overwrite it
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&acce[b]));
+    }
+    if (lane == 0) bulk_wait_read(0);  // shared memory stays until the stores have read it
+  }
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tmem_fence_after();
+    tmem_dealloc(tacc, 2 * kPqBN);
+  }
 }
 
 template <typename OutT>
@@ -319,21 +362,46 @@ size_t qk_smem_bytes(int head_dim, int bn) {
   return 1024 + (size_t)db * (kABlock + (size_t)bn * kKB * 2) + 64;
 }
 
+template <typename OutT>
+const void *qk_persistent_fn() {
+  return reinterpret_cast<const void *>(&fos_qk_persistent_kernel<OutT>);
+}
+
+const void *qk_persistent_fn_for(fos_dtype out) {
+  switch (out) {
+    case FOS_F32: return qk_persistent_fn<float>();
+    case FOS_BF16: return qk_persistent_fn<__nv_bfloat16>();
+    case FOS_F16: return qk_persistent_fn<__half>();
+  }
+  return nullptr;
+}
+
+size_t qk_persistent_smem_bytes(int head_dim) {
+  const int db = head_dim / kKB;
+  // alignment slack, two operand stages, the epilogue's staging, 8 barriers and the
+  // tensor-memory address
+  return 1024 + 2 * (size_t)db * (kABlock + kPqBN * kKB * 2) + kPqEpiWarps * 2 * kStage + 64 + 16;
+}
+
 fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *q,
                   const void *k, void *scores, cudaStream_t stream, unsigned *err,
-                  int max_smem) {
-  const int bn = d->tile_n ? d->tile_n : kQkDefaultTileN;
-  const size_t smem = qk_smem_bytes(d->head_dim, bn);
+                  int max_smem, int sms) {
+  const bool persistent = d->tile_n == 0;
+  const int bn = persistent ? kPqBN : d->tile_n;
+  const size_t smem = persistent ? qk_persistent_smem_bytes(d->head_dim)
+                                 : qk_smem_bytes(d->head_dim, bn);
   if (smem > (size_t)max_smem) return FOS_ERR_UNSUPPORTED;
+  const void *fn = persistent ? qk_persistent_fn_for(out_dt) : qk_fn_for(out_dt, bn);
   static std::mutex mu;
-  static bool prepared[3][2] = {};
+  static bool prepared[3][3] = {};
   {
+    const int kind = persistent ? 2 : (bn == 256);
     std::lock_guard<std::mutex> lock(mu);
-    if (!prepared[out_dt][bn == 256]) {
-      if (cudaFuncSetAttribute(qk_fn_for(out_dt, bn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               max_smem) != cudaSuccess)
+    if (!prepared[out_dt][kind]) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+          cudaSuccess)
         return FOS_ERR_CUDA;
-      prepared[out_dt][bn == 256] = true;
+      prepared[out_dt][kind] = true;
     }
   }
   const CUtensorMapDataType in_ty =
@@ -359,12 +427,22 @@ fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const
   a.scale = d->scale;
   a.timeout_ns = 2000000000ull;
   a.err = err;
-  const uint32_t idesc = qk_idesc(in_dt == FOS_BF16, bn);
+  const uint32_t idesc = f16_idesc(in_dt == FOS_BF16, kBM, bn, false);
+  if (persistent) {
+    QkTiles tl{};
+    tl.nx = (d->kv_len + kPqBN - 1) / kPqBN;
+    tl.ny = (d->q_len + kBM - 1) / kBM;
+    tl.ntiles = (int64_t)tl.nx * tl.ny * d->batch * d->q_heads;
+    const int grid = (int)(tl.ntiles < sms ? tl.ntiles : sms);
+    void *args[] = {&qm, &km, &sm, &a, &tl, const_cast<uint32_t *>(&idesc)};
+    if (cudaLaunchKernel(fn, dim3(grid), dim3(kPqThreads), args, smem, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+    return FOS_OK;
+  }
   const dim3 grid((unsigned)((d->kv_len + bn - 1) / bn), (unsigned)((d->q_len + kBM - 1) / kBM),
                   (unsigned)(d->batch * d->q_heads));
   void *args[] = {&qm, &km, &sm, &a, const_cast<uint32_t *>(&idesc)};
-  if (cudaLaunchKernel(qk_fn_for(out_dt, bn), grid, dim3(kQkThreads), args, smem, stream) !=
-      cudaSuccess)
+  if (cudaLaunchKernel(fn, grid, dim3(kQkThreads), args, smem, stream) != cudaSuccess)
     return FOS_ERR_CUDA;
   return FOS_OK;
 }

@@ -341,8 +341,10 @@ typedef struct fos_qk_desc {
   int32_t head_dim;   /* D: 64 or 128 */
   int64_t ld_scores;  /* elements between rows of scores, >= kv_len */
   float scale;        /* applied to the float32 sum (e.g. 1 / sqrt(D)) */
-  int32_t tile_n;     /* keys per CTA tile: 0 = default, 128 or 256 (no result bit depends on
-                         it; each score's sum is the same sequence of instructions) */
+  int32_t tile_n;     /* 0 = default: one CTA per SM walks 128 x 128 tiles, one tile's stores
+                         overlapping the next tile's copies and multiplies; 128 or 256: one CTA
+                         per tile of that many keys.  No result bit depends on it: each score's
+                         sum is the same sequence of instructions. */
 } fos_qk_desc;
 
 /*
@@ -355,11 +357,48 @@ typedef struct fos_qk_desc {
  * FOS_ERR_INVALID for a bad description (negative sizes, q_heads not a multiple of kv_heads,
  * ld_scores < kv_len, tile_n not 0, 128 or 256) or dtype; FOS_ERR_UNSUPPORTED for another head dimension
  * or more than 65535 (batch x query heads) or query tiles of 128.  A problem with no score is a
- * no-op.  Resources: each CTA allocates tile_n (128 by default) tensor-memory columns and frees
- * them before it exits.  A bounded wait that runs out is reported by fos_device_error() as FOS_ERR_TIMEOUT.
+ * no-op.  Resources: each CTA allocates 256 tensor-memory columns (tile_n columns with tile_n
+ * given) and frees them before it exits.  A bounded wait that runs out is reported by fos_device_error() as FOS_ERR_TIMEOUT.
  */
 fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
                          const void *q, const void *k, void *scores, cudaStream_t stream);
+
+/*
+ * The PV contraction behind the softmax: out[b, h, i, d] = sum_j probs[b, h, i, j] *
+ * v[b, h / (q_heads / kv_heads), j, d] on the tensor cores, the keys accumulated in float32 in a
+ * fixed order (steps of 16, ascending from key 0), rounded once to the output dtype.  Each
+ * output depends only on its probability row and the value rows, so it has the same bits
+ * whatever the batch, the heads around it or its row's position.  ("Batch-invariant attention
+ * (standard softmax--cuda version)", Fixed Reduction Contract: one writer per output, the keys
+ * in a fixed order; "[WS1][kernels] Add fixed-order joint-attention softmax for Qwen-Image",
+ * Summary: the softmax feeds the AV GEMM.)
+ */
+typedef struct fos_pv_desc {
+  int32_t batch;      /* B */
+  int32_t q_heads;    /* Hq, a multiple of kv_heads */
+  int32_t kv_heads;   /* Hkv >= 1; query head h reads value head h / (Hq / Hkv) */
+  int32_t q_len;      /* Sq */
+  int32_t kv_len;     /* Skv >= 1 */
+  int32_t head_dim;   /* D: 64 or 128 */
+  int64_t ld_probs;   /* elements between rows of probs, >= kv_len */
+} fos_pv_desc;
+
+/*
+ *   probs  device [batch][q_heads][q_len][ld_probs] of in_dtype (FOS_BF16 or FOS_F16): P, as the
+ *          forward writes it (columns kv_len .. ld_probs-1 are not read)
+ *   v      device [batch][kv_heads][kv_len][head_dim] of in_dtype, dense
+ *   out    device [batch][q_heads][q_len][head_dim] of out_dtype (FOS_F32, FOS_BF16, FOS_F16),
+ *          dense; must not overlap probs or v
+ * probs, v and out must start on 16-byte boundaries and ld_probs must be a multiple of 8
+ * (FOS_ERR_UNSUPPORTED otherwise).  FOS_ERR_INVALID for a bad description (negative sizes,
+ * kv_len < 1, q_heads not a multiple of kv_heads, ld_probs < kv_len) or dtype;
+ * FOS_ERR_UNSUPPORTED for another head dimension or more than 65535 (batch x query heads).  A
+ * problem with no output is a no-op.  Resources: each CTA allocates head_dim tensor-memory
+ * columns and frees them before it exits; a bounded wait that runs out is reported by
+ * fos_device_error() as FOS_ERR_TIMEOUT.
+ */
+fos_status fos_pv_out(const fos_pv_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
+                      const void *probs, const void *v, void *out, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reports and clears the device error word of the current

@@ -18,6 +18,10 @@ The bounds are the stated correctness bar of the kernels, read as follows:
   products, whatever its order, stays within (D - 1) * 2^-24 of that absolute sum, 2^-17 at
   D = 128; 2^-16 leaves room for the final multiply by the scale), plus one ULP of the FP64 value
   for a 16-bit output dtype (its single rounding).
+* PV outputs: the same form over the keys, |err| <= 2^-16 * sum_j |p_j v_jd| plus one ULP for a
+  16-bit output (the scale is 1).  Over thousands of keys the worst-case float32 bound is looser
+  than this, but the partial sums of terms of both signs stay far below the absolute sum, and the
+  bound is the one an accurate float32 sum in any fixed order meets on such data.
 * d_sink (float32): |err| <= 1e-5 * sum_r |c_r| with c_r = exp(sink_h - LSE_r) * delta_r.
 """
 
@@ -129,3 +133,8 @@ def check_scores(gpu, ref, abs_dot, scale, dtype: str):
     err = np.abs(gpu - ref)
     w, i = _worst(err, bound)
     return bool(np.all(err <= bound)), w, i
+
+
+def check_pv(gpu, ref, abs_dot, dtype: str):
+    """PV outputs; abs_dot = sum_j |p_j v_jd| per output (float64, same shape as ref)."""
+    return check_scores(gpu, ref, abs_dot, 1.0, dtype)

@@ -39,10 +39,11 @@ def check_against_oracle(q, k, s, scale, out_name):
 @pytest.mark.parametrize("in_name", ["bfloat16", "float16"])
 @pytest.mark.parametrize("out_name", ["float32", "bfloat16", "float16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [0, 128, 256])
 def test_scores_match_the_oracle(in_name, out_name, D, tile_n):
     # two query tiles (the second ragged) x two or three key tiles (the last ragged), grouped
-    # heads; 300 keys make 600-byte rows in a 16-bit output, so the binding pads the row stride
+    # heads; 300 keys make 600-byte rows in a 16-bit output, so the binding pads the row stride.
+    # tile_n 0: the persistent kernel (one CTA per SM over all tiles); 128 / 256: a CTA per tile
     B, Hq, Hkv, Sq, Skv = 2, 4, 2, 200, 300
     q, k = qk_inputs(B, Hq, Hkv, Sq, Skv, D, DTYPES[in_name], seed=D + 7)
     scale = 1.0 / math.sqrt(D)

@@ -203,3 +203,13 @@ def test_check_scores_bound(dtype, one):
     assert not tol.check_scores(ref - 1.01 * bound, ref, absd, 0.5, dtype)[0]
     # the scale's sign does not matter
     assert tol.check_scores(ref + 0.99 * bound, ref, absd, -0.5, dtype)[0]
+
+
+def test_check_pv_bound():
+    # output 2.0 with sum_j |p_j v_jd| = 4: floor 2^-16 * 4 = 2^-14, plus one bf16 ULP at 2 (2^-6)
+    ref = np.array([2.0])
+    absd = np.array([4.0])
+    for dtype, one in (("float32", 0.0), ("bfloat16", 2.0 ** -6)):
+        bound = 2.0 ** -14 + one
+        assert tol.check_pv(ref + 0.99 * bound, ref, absd, dtype)[0]
+        assert not tol.check_pv(ref + 1.01 * bound, ref, absd, dtype)[0]
