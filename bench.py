@@ -317,7 +317,7 @@ def run_reference(args):
 # 4,352 keys, padded prompts, causal rows with a sink, the large bf16 / fp32 case, the tiny
 # fp32 case); the headline `value` is the first.
 REPORTED = ["qwen_image_bf16", "prompt_padding_bf16", "sink_causal_bf16", "large_bf16",
-            "large_fp32", "tiny_fp32"]
+            "large_fp32", "tiny_fp32", "long_rows_bf16"]
 
 
 def sha256_rows(*tensors, rows=None):

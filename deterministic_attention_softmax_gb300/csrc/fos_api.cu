@@ -306,10 +306,30 @@ using namespace fos;
 
 namespace fos {
 
-// Rows longer than a shared-memory stage (or load_path 3): segments of this many tiles, read
-// twice, with this many compute warps by default.
+// Rows longer than a shared-memory stage (or load_path 3) are read twice in segments of
+// max(16, 2 x warps) tiles, so that every warp takes two tiles of a full segment.  Default
+// launches, measured on GB300 (1,024 rows of 262,144 bf16 keys; 8 / 12 / 16 / 24 / 31 compute
+// warps, 152 / 304 / 456 CTAs, rings of 2..6 segments; same bits throughout): the forward
+// recomputes its exponentials and is issue-bound, best with 12 warps, two CTAs per SM and six
+// segments in flight (328 us; 340 with 8 warps and three); the backward is bound by DRAM and
+// runs fastest with 16 warps, one CTA per SM and four segments (377 us; 400 with 8 warps):
+// fewer rows in flight leave more of each row in L2 for its second read.  Rows whose tile
+// statistics leave no room for that ring fall back to 8 warps and 16-tile segments.
 constexpr int kStreamSegTiles = 16;
-constexpr int kStreamWarps = 8;
+constexpr int kStreamWarpsFwd = 12;
+constexpr int kStreamStagesFwd = 6;
+constexpr int kStreamWarpsBwd = 16;
+constexpr int kStreamStagesBwd = 4;
+constexpr int kStreamWarpsNarrow = 8;
+
+int stream_seg_tiles(int warps) {
+  return 2 * warps > kStreamSegTiles ? 2 * warps : kStreamSegTiles;
+}
+
+// The ring bytes plan_rows may fill for a streaming launch: `stages` segments.
+size_t stream_ring_target(int seg_tiles, fos_dtype dt, int copies, int stages) {
+  return (size_t)stages * copies * seg_tiles * kTileK * dtype_size(dt);
+}
 
 bool stream_rows(const fos_desc *desc, fos_dtype dtype, int copies, size_t (*extra)(int, int),
                  const fos_launch *launch, const DevInfo &dev) {
@@ -505,13 +525,20 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   Plan pl;
   const void *inputs[1] = {scores};
   if (stream_rows(desc, dtype, 1, fwd_extra_smem, launch, *dev)) {
-    const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kStreamWarps;
-    st = plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev, fwd_extra_smem,
-                   warps, 24 * 1024, 0x300u | ((uint32_t)dtype << 4),
-                   [dtype](int th, size_t sm, int *n) {
-                     return fwd_stream_occupancy(dtype, th, sm, n);
-                   },
-                   &a, &pl, kStreamSegTiles);
+    const bool given = launch && launch->warps_per_cta;
+    auto plan = [&](int warps) {
+      const int seg = stream_seg_tiles(warps);
+      return plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev,
+                       fwd_extra_smem, warps,
+                       stream_ring_target(seg, dtype, 1, kStreamStagesFwd),
+                       0x300u | ((uint32_t)dtype << 4),
+                       [dtype](int th, size_t sm, int *n) {
+                         return fwd_stream_occupancy(dtype, th, sm, n);
+                       },
+                       &a, &pl, seg);
+    };
+    st = plan(given ? launch->warps_per_cta : kStreamWarpsFwd);
+    if (st == FOS_ERR_UNSUPPORTED && !given) st = plan(kStreamWarpsNarrow);
     if (st != FOS_OK) return st;
     a.scores = scores;
     a.probs = probs;
@@ -671,13 +698,20 @@ fos_status run_bwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
   Plan pl;
   const void *inputs[2] = {probs, dprobs};
   if (stream_rows(desc, dtype, 2, bwd_extra_smem, launch, *dev)) {
-    const int warps = (launch && launch->warps_per_cta) ? launch->warps_per_cta : kStreamWarps;
-    st = plan_rows(desc, dtype, row_base, nrows, inputs, 2, dscores, launch, *dev, bwd_extra_smem,
-                   warps, 48 * 1024, 0x400u | ((uint32_t)dtype << 4),
-                   [dtype](int th, size_t sm, int *n) {
-                     return bwd_stream_occupancy(dtype, th, sm, n);
-                   },
-                   &a, &pl, kStreamSegTiles);
+    const bool given = launch && launch->warps_per_cta;
+    auto plan = [&](int warps) {
+      const int seg = stream_seg_tiles(warps);
+      return plan_rows(desc, dtype, row_base, nrows, inputs, 2, dscores, launch, *dev,
+                       bwd_extra_smem, warps,
+                       stream_ring_target(seg, dtype, 2, kStreamStagesBwd),
+                       0x400u | ((uint32_t)dtype << 4),
+                       [dtype](int th, size_t sm, int *n) {
+                         return bwd_stream_occupancy(dtype, th, sm, n);
+                       },
+                       &a, &pl, seg);
+    };
+    st = plan(given ? launch->warps_per_cta : kStreamWarpsBwd);
+    if (st == FOS_ERR_UNSUPPORTED && !given) st = plan(kStreamWarpsNarrow);
     if (st != FOS_OK) return st;
     a.probs = probs;
     a.dprobs = dprobs;

@@ -152,13 +152,17 @@ __device__ __forceinline__ void grad_tiles(const unsigned char *sp, const unsign
 template <bool kOct>
 struct RowCursor;
 
+// Rows are taken from the last to the first.  The forward writes P from the first row to the
+// last, so a backward that follows it starts on the rows whose P the forward wrote last, the
+// likeliest to be still in L2.  The order of rows never changes a row's bits.
 template <>
 struct RowCursor<false> {
-  int64_t r;
-  __device__ RowCursor(const BwdArgs &, int64_t first) : r(first) {}
-  __device__ bool valid(const BwdArgs &a) const { return r < a.rows; }
-  __device__ int64_t row() const { return r; }
-  __device__ void next(const BwdArgs &, int64_t step) { r += step; }
+  int64_t k;     // rows counted from the last one
+  int64_t last;  // the launch's last row
+  __device__ RowCursor(const BwdArgs &a, int64_t first) : k(first), last(a.rows - 1) {}
+  __device__ bool valid(const BwdArgs &a) const { return k < a.rows; }
+  __device__ int64_t row() const { return last - k; }
+  __device__ void next(const BwdArgs &, int64_t step) { k += step; }
 };
 
 // The octet cursor moves from row to row incrementally: the next position of a head is the next
@@ -580,7 +584,8 @@ const void *bwd_rowwarp_fn(fos_dtype dt, bool sink = false) {
 // of P and dP that cycle through the ring; pass 1 takes the tile partials of delta segment by
 // segment, one thread adds them left to right, and pass 2 reads every segment again for
 // dScores.  The per-tile arithmetic and the order of the delta sum are those of
-// fos_bwd_kernel, so a row gives the same bits on either path.
+// fos_bwd_kernel, so a row gives the same bits on either path.  Rows are taken from the last
+// to the first, as in fos_bwd_kernel (the forward's last rows of P are the likeliest in L2).
 
 // Producer: each row's segments of P and dP twice (pass 1, then pass 2), with the row's record
 // beside every segment; a row with no valid key still gets one empty segment per pass.
@@ -597,7 +602,7 @@ __device__ void bwd_stream_produce(const BwdArgs &a, int64_t r0, int64_t G, int6
   int64_t n = 0;  // segments issued so far
   bool stop = false;
   for (int64_t kk = 0; kk < nmine && !stop; ++kk) {
-    const int64_t rr = r0 + kk * G;
+    const int64_t rr = a.rows - 1 - (r0 + kk * G);
     const int4 g = row_geometry(a, rr);
     const int nseg = g.x > 0 ? (g.x + seg_keys - 1) / seg_keys : 1;
     const size_t off = (size_t)rr * a.ld * esz;
@@ -679,7 +684,7 @@ __global__ void __maxnreg__(80) fos_bwd_stream_kernel(const BwdArgs a) {
   int s = 0;
   uint32_t ph = 0;
   for (int64_t k = 0; k < nmine; ++k) {
-    const int64_t r = r0 + k * G;
+    const int64_t r = a.rows - 1 - (r0 + k * G);
     bool timed_out = false;
     int lim = 0, Te = 0, nseg = 1;
     const uint8_t *km = nullptr;

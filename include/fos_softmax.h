@@ -21,10 +21,11 @@
  * buffers per warp); the arithmetic is the same, so the bits are too.
  *
  * Long rows.  A row is normally staged whole in shared memory (up to about 57k fp32 / 113k
- * bf16 keys forward, half that backward).  Longer rows are read twice, in segments of 16
- * tiles, by streaming kernels with the same per-tile arithmetic and merge order, so a row gives
- * the same bits either way; they need 16-byte aligned rows (base, ld * size and key_len * size
- * multiples of 16 bytes) and fit up to about 4.5 M (forward) / 14 M (backward) bf16 keys.
+ * bf16 keys forward, half that backward).  Longer rows are read twice, in segments of
+ * max(16, 2 x compute warps) tiles, by streaming kernels with the same per-tile arithmetic and
+ * merge order, so a row gives the same bits either way; they need 16-byte aligned rows (base,
+ * ld * size and key_len * size multiples of 16 bytes) and fit up to about 4.5 M (forward) /
+ * 14 M (backward) bf16 keys.
  *
  * Masks.  Key j of row r is valid iff all of the given conditions hold:
  *   causal:        j <= key_len - q_len + i
@@ -154,7 +155,11 @@ typedef struct fos_launch {
  * Resources: besides shared memory, each CTA of the forward allocates tensor memory (tcgen05,
  * at most 256 of an SM's 512 columns) for its lifetime, and it frees it before exiting, on
  * error paths too.  A kernel of another stream that holds the SM's remaining columns makes the
- * forward's CTAs wait in their allocation until those are released.
+ * forward's CTAs wait in their allocation until those are released.  No kernel of this library
+ * waits on another kernel while it holds columns (fos_qk_scores and fos_pv_out free theirs
+ * when their CTAs finish their own tiles), so such a wait between this library's kernels
+ * always ends; a caller's kernel that holds columns until the softmax has run would never
+ * see it run.
  */
 fos_status fos_softmax_fwd(const fos_desc *desc, fos_dtype dtype, const void *scores,
                            void *probs, float *lse, cudaStream_t stream,

@@ -1,8 +1,9 @@
 """Rows longer than a shared-memory stage: the streaming kernels read such a row twice, in
-segments of 16 tiles.  Their rows are checked against the FP64 oracle within the parity
-tolerances; on rows that also fit a stage, forcing the streaming kernels (load_path 3) must give
-the bits of the staged kernels, masks and sink included; and what they cannot take (unaligned
-rows, plain loads, tile statistics beyond shared memory) is refused before any launch."""
+segments of max(16, 2 x compute warps) tiles.  Their rows are checked against the FP64 oracle
+within the parity tolerances; on rows that also fit a stage, forcing the streaming kernels
+(load_path 3) must give the bits of the staged kernels, masks and sink included; and what they
+cannot take (unaligned rows, plain loads, tile statistics beyond shared memory) is refused before
+any launch."""
 
 import pytest
 import torch
@@ -56,6 +57,25 @@ def test_streaming_bits_do_not_depend_on_its_geometry(dtype, warps, stages):
     (a, b) = both_paths(c, dtype, None, fos.Launch(load_path=3, warps_per_cta=warps, stages=stages))
     for x, y in zip(a, b):
         assert bits_equal(x, y)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+@pytest.mark.parametrize("extra", [-1, 0, 1, 5])
+@pytest.mark.parametrize("warps", [8, 12])
+def test_segments_through_the_ring_give_the_staged_bits(stages, extra, warps):
+    # Rows of fewer, as many and more segments than the ring has stages (segments of 16 tiles
+    # with 8 warps, 24 with 12; the last one ragged), with valid lengths that give the rows of
+    # one launch different segment counts: the stage and phase of every segment, in both
+    # passes, cycle through the ring across rows of different lengths
+    nseg = max(1, stages + extra)
+    seg_keys = 256 * max(16, 2 * warps)
+    L = seg_keys * (nseg - 1) + 1000
+    c = make_case(torch.bfloat16, L, "all", B=2, H=2, Sq=3, seed=nseg + 10 * warps)
+    (a, b) = both_paths(c, torch.bfloat16, None,
+                        fos.Launch(load_path=3, warps_per_cta=warps, stages=stages))
+    for x, y, name in zip(a, b, ("P", "LSE", "dScores", "delta")):
+        assert bits_equal(x, y), f"{name} L={L} stages={stages} warps={warps}"
+    assert fos.fos_device_error() == 0
 
 
 def test_what_streaming_cannot_take_is_refused():
