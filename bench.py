@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
     ap.add_argument("--workload-iters", type=int, default=20)
-    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "pv"],
+    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "qk_bf16", "pv"],
                     default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
@@ -883,11 +883,12 @@ def run_profile(args):
         torch.cuda.synchronize()
         assert fos.fos_device_error() == 0
         return
-    if args.profile == "qk":  # the QK contraction on the Qwen-Image shape (float32 scores)
+    if args.profile in ("qk", "qk_bf16"):  # the QK contraction on the Qwen-Image shape
+        odt = torch.float32 if args.profile == "qk" else torch.bfloat16
         g = torch.Generator(device=dev).manual_seed(61)
         q = torch.randn(1, 4, 4096, 128, generator=g, device=dev).to(torch.bfloat16)
         k = torch.randn(1, 4, 4352, 128, generator=g, device=dev).to(torch.bfloat16)
-        s = fos.fos_qk_scores(q, k, 0.0884)
+        s = fos.fos_qk_scores(q, k, 0.0884, out_dtype=odt)
         for _ in range(args.warmup + args.steps):
             fos.fos_qk_scores(q, k, 0.0884, scores=s)
         torch.cuda.synchronize()

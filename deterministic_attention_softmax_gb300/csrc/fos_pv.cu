@@ -33,7 +33,7 @@ constexpr int kPvBM = 128;     // query rows per CTA (MMA M)
 constexpr int kPvKB = 64;      // keys per block (128 bytes of bf16 along K in the P tile)
 constexpr int kPvUK = 16;      // keys per MMA
 constexpr int kPvThreads = 128;
-constexpr int kPvStages = 4;
+constexpr int kPvStages = 6;
 constexpr int kPvABytes = kPvBM * kPvKB * 2;  // 16 KB
 constexpr int kPvBHalf = kPvKB * 64 * 2;      // 8 KB: 64 keys x 64 value columns
 constexpr int kPvStage = 32 * 128;            // epilogue staging block: 32 rows x 128 bytes

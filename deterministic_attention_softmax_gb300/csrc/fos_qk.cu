@@ -172,18 +172,27 @@ __global__ void __launch_bounds__(kQkThreads, 1)
 }
 
 // ---- persistent form: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... of
-// 128 x 128 scores (key tile fastest).  Warp 0 issues the copies into two operand stages, warp 1
-// the MMAs into two accumulators (2 x 128 tensor-memory columns), warps 2..9 drain an
-// accumulator (two warps per lane quarter, 64 columns each) while the next tile's copies and
-// MMAs proceed.  Each tile's scores are the same instructions on the same operands as in
-// fos_qk_kernel, so the bits are the same.
+// 128 x 128 scores (key tile fastest), so that the CTAs of the grid write one compact band of
+// the output at a time.  Warp 0 issues the copies into a ring of `stages` operand stages (a
+// tile's Q and K blocks are reloaded, mostly from L2; three stages at D = 128), warp 1 the MMAs
+// into kPqAcc accumulators of 128 tensor-memory columns, and warps 2..5 drain an accumulator
+// (one warp per lane quarter, all 128 columns) while the MMAs of the next tiles proceed into
+// the other accumulators.  Measured on the Qwen-Image shape against two stages, two
+// accumulators and eight epilogue warps (two per lane quarter): float32 scores 53.3 -> 51.7 us,
+// bf16 38.9 -> 37.3 us.  Each tile's scores are the same instructions on the same operands as
+// in fos_qk_kernel, so the bits are the same.
 constexpr int kPqBN = 128;
-constexpr int kPqThreads = 320;
-constexpr int kPqEpiWarps = 8;
+constexpr int kPqEpiWarps = 4;
+constexpr int kPqEpiCols = kPqBN * 4 / kPqEpiWarps;  // columns per epilogue warp
+constexpr int kPqAcc = 4;
+constexpr int kPqThreads = (2 + kPqEpiWarps) * 32;
+constexpr int kPqMaxStages = 4;
+static_assert(kPqEpiWarps == 4 || kPqEpiWarps == 8, "one or two warps per lane quarter");
 
 struct QkTiles {
   int32_t nx, ny;  // key tiles, query tiles per (batch, head)
   int64_t ntiles;  // nx * ny * batch * q_heads
+  int32_t stages;  // operand stages (2 .. kPqMaxStages)
 };
 
 template <typename OutT>
@@ -196,23 +205,27 @@ __global__ void __launch_bounds__(kPqThreads, 1)
   constexpr int kBBlock = kPqBN * kKB * 2;  // 16 KB
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int NS = tl.stages;
   const int stage_bytes = a.dblocks * (kABlock + kBBlock);
-  unsigned char *staging = smem + 2 * stage_bytes;  // 8 warps x 2 x 4 KB
+  unsigned char *staging = smem + NS * stage_bytes;  // epilogue warps x 2 x 4 KB
   uint64_t *bars = reinterpret_cast<uint64_t *>(staging + kPqEpiWarps * 2 * kStage);
-  uint64_t *full = bars, *empty = bars + 2, *accf = bars + 4, *acce = bars + 6;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8);
+  uint64_t *full = bars, *empty = bars + kPqMaxStages, *accf = bars + 2 * kPqMaxStages,
+           *acce = accf + kPqAcc;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + kPqAcc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
       mbar_init(smem_addr(&empty[i]), 1);
+    }
+    for (int i = 0; i < kPqAcc; ++i) {
       mbar_init(smem_addr(&accf[i]), 1);
       mbar_init(smem_addr(&acce[i]), kPqEpiWarps);
     }
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 2 * kPqBN);
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), kPqAcc * kPqBN);
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
@@ -223,9 +236,9 @@ __global__ void __launch_bounds__(kPqThreads, 1)
     if (lane == 0) {  // ---- copies
       int64_t i = 0;
       for (int64_t t = blockIdx.x; t < tl.ntiles; t += gridDim.x, ++i) {
-        const int s = (int)(i & 1);
-        if (i >= 2 && !mbar_wait_bounded(smem_addr(&empty[s]), (uint32_t)((i >> 1) & 1) ^ 1u,
-                                         a.timeout_ns)) {
+        const int s = (int)(i % NS);
+        if (i >= NS && !mbar_wait_bounded(smem_addr(&empty[s]), (uint32_t)((i / NS) & 1) ^ 1u,
+                                          a.timeout_ns)) {
           raise_device_error(a.err, kDevErrTimeout);
           break;
         }
@@ -244,20 +257,21 @@ __global__ void __launch_bounds__(kPqThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // ---- MMAs: tile i into accumulator i % 2, head dimension ascending
+    if (lane == 0) {  // ---- MMAs: tile i into accumulator i % kPqAcc, head dimension ascending
       int64_t i = 0;
       for (int64_t t = blockIdx.x; t < tl.ntiles; t += gridDim.x, ++i) {
-        const int s = (int)(i & 1);
-        if (!mbar_wait_bounded(smem_addr(&full[s]), (uint32_t)((i >> 1) & 1), a.timeout_ns) ||
-            (i >= 2 && !mbar_wait_bounded(smem_addr(&acce[s]), (uint32_t)((i >> 1) & 1) ^ 1u,
-                                          a.timeout_ns))) {
+        const int s = (int)(i % NS), b = (int)(i % kPqAcc);
+        if (!mbar_wait_bounded(smem_addr(&full[s]), (uint32_t)((i / NS) & 1), a.timeout_ns) ||
+            (i >= kPqAcc &&
+             !mbar_wait_bounded(smem_addr(&acce[b]), (uint32_t)((i / kPqAcc) & 1) ^ 1u,
+                                a.timeout_ns))) {
           raise_device_error(a.err, kDevErrTimeout);
           break;
         }
         tmem_fence_after();
         unsigned char *sa = smem + s * stage_bytes;
         unsigned char *sb = sa + a.dblocks * kABlock;
-        const uint32_t dacc = tacc + (uint32_t)(s * kPqBN);
+        const uint32_t dacc = tacc + (uint32_t)(b * kPqBN);
         for (int kb = 0; kb < a.dblocks; ++kb)
           for (int k = 0; k < kKB / kUK; ++k) {
             const uint64_t ad = sw128_desc(smem_addr(sa + kb * kABlock + k * kUK * 2));
@@ -265,20 +279,21 @@ __global__ void __launch_bounds__(kPqThreads, 1)
             mma_f16(dacc, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
         mma_commit(smem_addr(&empty[s]));  // the stage may be refilled
-        mma_commit(smem_addr(&accf[s]));   // the accumulator may be drained
+        mma_commit(smem_addr(&accf[b]));   // the accumulator may be drained
       }
     }
   } else {
-    // ---- epilogue: warp w drains lane quarter w % 4, columns 64 * ((w - 2) / 4) .. + 63
+    // ---- epilogue: warp w drains lane quarter w % 4, kPqEpiCols columns from
+    // kPqEpiCols * ((w - 2) / 4)
     constexpr int kCols = 128 / (int)sizeof(OutT);  // 32 float or 64 bf16 / fp16 columns
-    const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
+    const int ew = warp - 2, quarter = warp & 3, c0 = (ew >> 2) * kPqEpiCols;
     unsigned char *stage0 = staging + ew * 2 * kStage;
     int nst = 0;  // stores issued by this warp
     int64_t i = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < tl.ntiles && ok; t += gridDim.x, ++i) {
-      const int b = (int)(i & 1);
-      ok = __all_sync(kFull, mbar_wait_bounded(smem_addr(&accf[b]), (uint32_t)((i >> 1) & 1),
+      const int b = (int)(i % kPqAcc);
+      ok = __all_sync(kFull, mbar_wait_bounded(smem_addr(&accf[b]), (uint32_t)((i / kPqAcc) & 1),
                                                a.timeout_ns));
       if (!ok) {
         if (lane == 0) raise_device_error(a.err, kDevErrTimeout);
@@ -288,8 +303,9 @@ __global__ void __launch_bounds__(kPqThreads, 1)
       const int zq = (int)(t / per_z);
       const int rem = (int)(t - (int64_t)zq * per_z);
       const int y = rem / tl.nx, x = rem - y * tl.nx;
-      const uint32_t trow = tacc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kPqBN + half * 64);
-      for (int c = 0; c < 64 / kCols; ++c, ++nst) {
+      const uint32_t trow =
+          tacc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kPqBN + c0);
+      for (int c = 0; c < kPqEpiCols / kCols; ++c, ++nst) {
         unsigned char *st = stage0 + (nst & 1) * kStage;
         if (lane == 0 && nst >= 2) bulk_wait_read(1);
         __syncwarp();
@@ -318,12 +334,12 @@ __global__ void __launch_bounds__(kPqThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store3(&smap, x * kPqBN + half * 64 + c * kCols, y * kBM + quarter * 32, zq,
+          tma_store3(&smap, x * kPqBN + c0 + c * kCols, y * kBM + quarter * 32, zq,
                      smem_addr(st));
           bulk_commit();
         }
       }
-      // this warp is done reading the accumulator: the MMAs of tile i + 2 may overwrite it
+      // this warp is done reading the accumulator: the MMAs of tile i + kPqAcc may overwrite it
       tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&acce[b]));
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(kPqThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tmem_fence_after();
-    tmem_dealloc(tacc, 2 * kPqBN);
+    tmem_dealloc(tacc, kPqAcc * kPqBN);
   }
 }
 
@@ -376,11 +392,19 @@ const void *qk_persistent_fn_for(fos_dtype out) {
   return nullptr;
 }
 
-size_t qk_persistent_smem_bytes(int head_dim) {
+// Shared memory of the persistent form with `stages` operand stages: alignment slack, the
+// stages, the epilogue's staging, the barriers and the tensor-memory address.
+size_t qk_persistent_smem_bytes(int head_dim, int stages) {
   const int db = head_dim / kKB;
-  // alignment slack, two operand stages, the epilogue's staging, 8 barriers and the
-  // tensor-memory address
-  return 1024 + 2 * (size_t)db * (kABlock + kPqBN * kKB * 2) + kPqEpiWarps * 2 * kStage + 64 + 16;
+  return 1024 + (size_t)stages * db * (kABlock + kPqBN * kKB * 2) + kPqEpiWarps * 2 * kStage +
+         (2 * kPqMaxStages + 2 * kPqAcc) * 8 + 16;
+}
+
+// The deepest operand ring (up to kPqMaxStages) that fits `max_smem`; 0 if not even two do.
+int qk_persistent_stages(int head_dim, int max_smem) {
+  for (int ns = kPqMaxStages; ns >= 2; --ns)
+    if (qk_persistent_smem_bytes(head_dim, ns) <= (size_t)max_smem) return ns;
+  return 0;
 }
 
 fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *q,
@@ -388,7 +412,9 @@ fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const
                   int max_smem, int sms) {
   const bool persistent = d->tile_n == 0;
   const int bn = persistent ? kPqBN : d->tile_n;
-  const size_t smem = persistent ? qk_persistent_smem_bytes(d->head_dim)
+  const int stages = persistent ? qk_persistent_stages(d->head_dim, max_smem) : 0;
+  if (persistent && stages == 0) return FOS_ERR_UNSUPPORTED;
+  const size_t smem = persistent ? qk_persistent_smem_bytes(d->head_dim, stages)
                                  : qk_smem_bytes(d->head_dim, bn);
   if (smem > (size_t)max_smem) return FOS_ERR_UNSUPPORTED;
   const void *fn = persistent ? qk_persistent_fn_for(out_dt) : qk_fn_for(out_dt, bn);
@@ -433,6 +459,7 @@ fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const
     tl.nx = (d->kv_len + kPqBN - 1) / kPqBN;
     tl.ny = (d->q_len + kBM - 1) / kBM;
     tl.ntiles = (int64_t)tl.nx * tl.ny * d->batch * d->q_heads;
+    tl.stages = stages;
     const int grid = (int)(tl.ntiles < sms ? tl.ntiles : sms);
     void *args[] = {&qm, &km, &sm, &a, &tl, const_cast<uint32_t *>(&idesc)};
     if (cudaLaunchKernel(fn, dim3(grid), dim3(kPqThreads), args, smem, stream) != cudaSuccess)

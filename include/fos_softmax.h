@@ -360,10 +360,12 @@ typedef struct fos_qk_desc {
  * q, k and scores must start on 16-byte boundaries and ld_scores * (size of out_dtype) must be
  * a multiple of 16 (FOS_ERR_UNSUPPORTED otherwise); scores must not overlap q or k.
  * FOS_ERR_INVALID for a bad description (negative sizes, q_heads not a multiple of kv_heads,
- * ld_scores < kv_len, tile_n not 0, 128 or 256) or dtype; FOS_ERR_UNSUPPORTED for another head dimension
- * or more than 65535 (batch x query heads) or query tiles of 128.  A problem with no score is a
- * no-op.  Resources: each CTA allocates 256 tensor-memory columns (tile_n columns with tile_n
- * given) and frees them before it exits.  A bounded wait that runs out is reported by fos_device_error() as FOS_ERR_TIMEOUT.
+ * ld_scores < kv_len, tile_n not 0, 128 or 256) or dtype; FOS_ERR_UNSUPPORTED for another
+ * head dimension or more than 65535 (batch x query heads) or query tiles of 128.  A problem with no score is a
+ * no-op.  Resources: with tile_n = 0, one CTA per SM that allocates all 512 tensor-memory
+ * columns (four accumulators); with tile_n given, tile_n columns per CTA.  Every CTA frees its
+ * columns before it exits.  A bounded wait that runs out is reported by fos_device_error() as
+ * FOS_ERR_TIMEOUT.
  */
 fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
                          const void *q, const void *k, void *scores, cudaStream_t stream);

@@ -53,6 +53,25 @@ def test_scores_match_the_oracle(in_name, out_name, D, tile_n):
     check_against_oracle(q, k, s, scale, out_name)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("out_name", ["float32", "bfloat16"])
+def test_runs_of_tiles_that_cross_query_tiles_and_heads(D, out_name):
+    # 8 query tiles (the last ragged) x 16 key tiles (the last ragged) x 4 batch-heads = 512
+    # tiles: the persistent kernel gives each CTA a contiguous run of three or four, so runs
+    # cross key tiles, query tiles (a new Q block mid-run) and batch-head boundaries, with
+    # grouped heads; every score against the oracle
+    B, Hq, Hkv, Sq, Skv = 2, 2, 1, 1000, 2000
+    q, k = qk_inputs(B, Hq, Hkv, Sq, Skv, D, torch.bfloat16, seed=D + 31)
+    scale = 1.0 / math.sqrt(D)
+    s = fos.fos_qk_scores(q, k, scale, out_dtype=DTYPES[out_name])
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+    check_against_oracle(q, k, s, scale, out_name)
+    # and the bits of the CTA-per-tile kernel (same instructions on the same operands)
+    s128 = fos.fos_qk_scores(q, k, scale, out_dtype=DTYPES[out_name], tile_n=128)
+    assert bits_equal(s.contiguous(), s128.contiguous())
+
+
 def test_qwen_image_shape_sampled():
     # the benchmark's shape: 16,384 query rows (4 heads x 4,096) against 4,352 keys, D = 128,
     # bf16 in, float32 scores; every score of a sample of query rows against the oracle
