@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
     ap.add_argument("--workload-iters", type=int, default=20)
-    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "qk_bf16", "pv"],
+    ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "qk_bf16", "pv",
+                                          "grad_kv"],
                     default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
@@ -504,7 +505,9 @@ def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
     4,096) against 4,352 keys, head dimension 128, bf16 Q and K, float32 and bf16 scores.  A
     parity gate on sampled query rows, then cold CUDA-event medians (512 MB scratch read before
     each launch).  Roofline: HBM (the score writes dominate: 64 flops per float32 score byte,
-    far below the tensor cores' ratio), with the tensor-core rate reported beside it."""
+    far below the tensor cores' ratio), with the tensor-core rate reported beside it.  The PV
+    contraction (P V) and the value gradient (dV = P^T dO, the key / value gradient kernel) on
+    the same shape, each behind its own parity gate, the same way."""
     import numpy as np
     import torch
 
@@ -591,7 +594,7 @@ def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
     from deterministic_attention_softmax_gb300 import _abi
 
     lib = _abi.lib()
-    d = _abi.FosPvDesc(B, H, H, Sq, Skv, D, pm.stride(2))
+    d = _abi.FosPvDesc(B, H, H, Sq, Skv, D, pm.stride(2), 1.0)
     sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     args = (ctypes.byref(d), _abi.FOS_BF16, _abi.FOS_F32, ctypes.c_void_p(pm.data_ptr()),
             ctypes.c_void_p(vv.data_ptr()), ctypes.c_void_p(o.data_ptr()), sh)
@@ -617,7 +620,45 @@ def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
                "algorithmic_bytes": nbytes, "out": "float32",
                "parity_gate": {"rows": int(len(rows)), "worst_err_over_bound": worst}})
     out["pv_out"] = pv
-    del q, k, scratch, pm, vv, o
+    # ---- the value gradient dV = P^T dO on the same shape (the key / value gradient kernel)
+    dout = torch.randn(B, H, Sq, D, generator=g2, device=dev).to(torch.bfloat16)
+    kvg = {"flops_per_launch": 2.0 * B * H * Sq * Skv * D}
+    dvo = fos.fos_grad_kv(pm, dout, H)
+    keys = np.unique(np.concatenate([[0, Skv - 1],
+                                     np.random.default_rng(3).integers(0, Skv, 24)]))
+    kt = torch.from_numpy(keys).to(dev)
+    pn_k, don = pm[..., kt].double().cpu().numpy(), dout.double().cpu().numpy()
+    zv = np.zeros((B, H, len(keys), D))
+    ok, worst, _ = tol.check_pv(dvo[:, :, kt].double().cpu().numpy(),
+                                gemm.pv_backward(don, pn_k, zv)[1],
+                                gemm.pv_backward(np.abs(don), np.abs(pn_k), zv)[1], "float32")
+    if not ok:
+        raise SystemExit(f"key / value gradient parity gate failed: worst {worst}")
+    args = (ctypes.byref(d), _abi.FOS_BF16, _abi.FOS_F32, ctypes.c_void_p(pm.data_ptr()),
+            ctypes.c_void_p(dout.data_ptr()), ctypes.c_void_p(dvo.data_ptr()), sh)
+    evs = []
+    for it in range(warmup + iters):
+        scratch.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if lib.fos_grad_kv(*args) != _abi.FOS_OK:
+            raise SystemExit("fos_grad_kv failed while timing")
+        e1.record()
+        if it >= warmup:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    if fos.fos_device_error() != 0:
+        raise SystemExit("device error while timing the key / value gradient contraction")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    nbytes = pm.numel() * 2 + dout.numel() * 2 + dvo.numel() * 4
+    kvg.update({"cold_ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                "tflops": kvg["flops_per_launch"] / (ms * 1e-3) / 1e12,
+                "frac_of_bf16_tensor": kvg["flops_per_launch"] / (ms * 1e-3) / 1e12 / tflops_peak,
+                "algorithmic_bytes": nbytes, "out": "float32", "what": "dV = P^T dO",
+                "parity_gate": {"keys": int(len(keys)), "worst_err_over_bound": worst}})
+    out["grad_kv"] = kvg
+    del q, k, scratch, pm, vv, o, dout, dvo
     torch.cuda.empty_cache()
     return out
 
@@ -873,6 +914,16 @@ def run_profile(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fos.build()
+    if args.profile == "grad_kv":  # dV = P^T dO on the Qwen-Image shape (float32 outputs)
+        g = torch.Generator(device=dev).manual_seed(63)
+        pm = torch.rand(1, 4, 4096, 4352, generator=g, device=dev).to(torch.bfloat16)
+        dout = torch.randn(1, 4, 4096, 128, generator=g, device=dev).to(torch.bfloat16)
+        o = fos.fos_grad_kv(pm, dout, 4)
+        for _ in range(args.warmup + args.steps):
+            fos.fos_grad_kv(pm, dout, 4, out=o)
+        torch.cuda.synchronize()
+        assert fos.fos_device_error() == 0
+        return
     if args.profile == "pv":  # the PV contraction on the Qwen-Image shape (float32 outputs)
         g = torch.Generator(device=dev).manual_seed(62)
         pm = torch.rand(1, 4, 4096, 4352, generator=g, device=dev).to(torch.bfloat16)

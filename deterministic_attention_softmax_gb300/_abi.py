@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "FOS_OK", 1: "FOS_ERR_INVALID", 2: "FOS_ERR_UNSUPPORTED", 3: 
 EXPORTED = ("fos_softmax_fwd", "fos_softmax_bwd", "fos_sink_grad", "fos_sink_grad_partials",
             "fos_sink_grad_merge", "fos_softmax_step_host",
             "fos_step_host_workspace_bytes", "fos_softmax_step_host_static", "fos_qk_scores",
-            "fos_pv_out",
+            "fos_pv_out", "fos_grad_kv",
             "fos_softmax_bwd_sink", "fos_bwd_sink_workspace_bytes", "fos_device_error",
             "fos_status_string", "fos_contract_fingerprint")
 
@@ -73,6 +73,7 @@ class FosPvDesc(ctypes.Structure):
         ("kv_len", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("ld_probs", ctypes.c_int64),
+        ("scale", ctypes.c_float),
     ]
 
 
@@ -137,6 +138,9 @@ def lib() -> ctypes.CDLL:
         L.fos_pv_out.argtypes = [ctypes.POINTER(FosPvDesc), ctypes.c_int, ctypes.c_int, vp, vp, vp,
                                  vp]
         L.fos_pv_out.restype = ctypes.c_int
+        L.fos_grad_kv.argtypes = [ctypes.POINTER(FosPvDesc), ctypes.c_int, ctypes.c_int, vp, vp,
+                                  vp, ctypes.c_void_p]
+        L.fos_grad_kv.restype = ctypes.c_int
         L.fos_device_error.argtypes = [vp]
         L.fos_device_error.restype = ctypes.c_int
         L.fos_status_string.argtypes = [ctypes.c_int]

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfos_softmax.so")
 SOURCES = ["fos_api.cu", "fos_fwd.cu", "fos_bwd.cu", "fos_sink.cu", "fos_host.cu", "fos_qk.cu",
-           "fos_pv.cu"]
+           "fos_pv.cu", "fos_kvgrad.cu"]
 HEADERS = [os.path.join(CSRC, "fos_device.cuh"), os.path.join(CSRC, "fos_internal.h"),
            os.path.join(CSRC, "fos_tc.cuh"),
            os.path.join(ROOT, "include", "fos_softmax.h")]

@@ -436,10 +436,10 @@ def fos_qk_scores(q, k, scale: float = 1.0, scores=None, *, out_dtype=torch.floa
     return scores
 
 
-def fos_pv_out(probs, v, out=None, *, out_dtype=torch.float32, stream=None):
-    """Output ``[B, Hq, Sq, D]`` = P V on the tensor cores (see ``fos_pv_out`` in the C header).
-    ``probs`` is a ``[B, Hq, Sq, Skv]`` view whose rows are ``ld`` elements apart (``ld`` a
-    multiple of 8), ``v`` a dense ``[B, Hkv, Skv, D]`` of the same 16-bit dtype."""
+def fos_pv_out(probs, v, out=None, *, scale: float = 1.0, out_dtype=torch.float32, stream=None):
+    """Output ``[B, Hq, Sq, D]`` = scale * P V on the tensor cores (see ``fos_pv_out`` in the C
+    header).  ``probs`` is a ``[B, Hq, Sq, Skv]`` view whose rows are ``ld`` elements apart
+    (``ld`` a multiple of 8), ``v`` a dense ``[B, Hkv, Skv, D]`` of the same 16-bit dtype."""
     if probs.dtype not in (torch.bfloat16, torch.float16) or v.dtype != probs.dtype:
         raise ValueError("probs and v must share one dtype, bfloat16 or float16")
     if probs.dim() != 4 or v.dim() != 4 or not v.is_contiguous() or probs.stride(-1) != 1:
@@ -461,12 +461,51 @@ def fos_pv_out(probs, v, out=None, *, out_dtype=torch.float32, stream=None):
     ld = probs.stride(2)
     if probs.stride(1) != Sq * ld or probs.stride(0) != Hq * Sq * ld:
         raise ValueError("probs rows must be one stride apart and densely packed otherwise")
-    d = _abi.FosPvDesc(B, Hq, Hkv, Sq, Skv, D, ld)
+    d = _abi.FosPvDesc(B, Hq, Hkv, Sq, Skv, D, ld, float(scale))
     with torch.cuda.device(dev):
         st = _abi.lib().fos_pv_out(ctypes.byref(d), _DTYPES[probs.dtype], _DTYPES[out.dtype],
                                    _ptr(probs), _ptr(v), _ptr(out), _stream_handle(stream, dev))
     if st != _abi.FOS_OK:
         raise FosError(st, "fos_pv_out")
+    return out
+
+
+def fos_grad_kv(a, m, kv_heads: int, scale: float = 1.0, out=None, *, out_dtype=torch.float32,
+                stream=None):
+    """Output ``[B, Hkv, Skv, D]`` = scale * a^T m summed over each key head's query heads (see
+    ``fos_grad_kv`` in the C header): dV from ``(P, dO)``, dK from ``(dScores, Q, scale)``.
+    ``a`` is a ``[B, Hq, Sq, Skv]`` view whose rows are ``ld`` elements apart (``ld`` a multiple
+    of 8), ``m`` a dense ``[B, Hq, Sq, D]`` of the same 16-bit dtype."""
+    if a.dtype not in (torch.bfloat16, torch.float16) or m.dtype != a.dtype:
+        raise ValueError("a and m must share one dtype, bfloat16 or float16")
+    if a.dim() != 4 or m.dim() != 4 or not m.is_contiguous() or a.stride(-1) != 1:
+        raise ValueError("a must be [B, Hq, Sq, Skv] with unit key stride, m dense [B, Hq, Sq, D]")
+    B, Hq, Sq, Skv = a.shape
+    Bm, Hm, Sm, D = m.shape
+    if (Bm, Hm, Sm) != (B, Hq, Sq):
+        raise ValueError("a and m must agree in batch, query heads and query positions")
+    kv_heads = int(kv_heads)
+    if kv_heads < 1 or Hq % kv_heads != 0:
+        raise ValueError("kv_heads must divide the query heads")
+    dev = a.device
+    _check_cuda(m, "m", dev)
+    if out is None:
+        out = torch.empty((B, kv_heads, Skv, D), dtype=out_dtype, device=dev)
+    if out.dtype not in _DTYPES or tuple(out.shape) != (B, kv_heads, Skv, D) or \
+            not out.is_contiguous():
+        raise ValueError("out must be a dense [B, Hkv, Skv, D] tensor")
+    _check_cuda(out, "out", dev)
+    if out.numel() == 0:
+        return out
+    ld = a.stride(2) if Sq > 0 else max(Skv, a.stride(2))
+    if Sq > 0 and (a.stride(1) != Sq * ld or a.stride(0) != Hq * Sq * ld):
+        raise ValueError("a rows must be one stride apart and densely packed otherwise")
+    d = _abi.FosPvDesc(B, Hq, kv_heads, Sq, Skv, D, ld, float(scale))
+    with torch.cuda.device(dev):
+        st = _abi.lib().fos_grad_kv(ctypes.byref(d), _DTYPES[a.dtype], _DTYPES[out.dtype],
+                                    _ptr(a), _ptr(m), _ptr(out), _stream_handle(stream, dev))
+    if st != _abi.FOS_OK:
+        raise FosError(st, "fos_grad_kv")
     return out
 
 

@@ -7,6 +7,7 @@
 #include <limits.h>
 #include <stdint.h>
 
+#include <cmath>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -885,7 +886,8 @@ extern "C" fos_status fos_pv_out(const fos_pv_desc *desc, fos_dtype in_dtype,
   if (desc == nullptr) return FOS_ERR_INVALID;
   const fos_pv_desc &d = *desc;
   if (d.batch < 0 || d.q_heads < 0 || d.kv_heads < 1 || d.q_len < 0 || d.kv_len < 1 ||
-      d.head_dim < 1 || d.ld_probs < d.kv_len || d.q_heads % d.kv_heads != 0)
+      d.head_dim < 1 || d.ld_probs < d.kv_len || d.q_heads % d.kv_heads != 0 ||
+      !(std::isfinite(d.scale) && d.scale != 0.0f))
     return FOS_ERR_INVALID;
   if (in_dtype != FOS_BF16 && in_dtype != FOS_F16) return FOS_ERR_INVALID;
   if (out_dtype != FOS_F32 && out_dtype != FOS_BF16 && out_dtype != FOS_F16) return FOS_ERR_INVALID;
@@ -899,6 +901,35 @@ extern "C" fos_status fos_pv_out(const fos_pv_desc *desc, fos_dtype in_dtype,
   fos_status st = device_info(&dev);
   if (st != FOS_OK) return st;
   return run_pv(desc, in_dtype, out_dtype, probs, v, out, stream, dev->err, dev->max_smem);
+}
+
+extern "C" fos_status fos_grad_kv(const fos_pv_desc *desc, fos_dtype in_dtype,
+                                  fos_dtype out_dtype, const void *a, const void *m, void *out,
+                                  cudaStream_t stream) {
+  if (desc == nullptr) return FOS_ERR_INVALID;
+  const fos_pv_desc &d = *desc;
+  if (d.batch < 0 || d.q_heads < 0 || d.kv_heads < 1 || d.q_len < 0 || d.kv_len < 0 ||
+      d.head_dim < 1 || d.ld_probs < d.kv_len || d.q_heads % d.kv_heads != 0 || d.q_heads < 1 ||
+      !(std::isfinite(d.scale) && d.scale != 0.0f))
+    return FOS_ERR_INVALID;
+  if (in_dtype != FOS_BF16 && in_dtype != FOS_F16) return FOS_ERR_INVALID;
+  if (out_dtype != FOS_F32 && out_dtype != FOS_BF16 && out_dtype != FOS_F16) return FOS_ERR_INVALID;
+  const int64_t nout = (int64_t)d.batch * d.kv_heads * d.kv_len * d.head_dim;
+  if (nout == 0) return FOS_OK;
+  if (out == nullptr) return FOS_ERR_INVALID;
+  if (d.head_dim != 64 && d.head_dim != 128) return FOS_ERR_UNSUPPORTED;
+  if (d.q_len == 0)  // a sum over no query position: every output is +0
+    return cudaMemsetAsync(out, 0, (size_t)nout * dtype_size(out_dtype), stream) == cudaSuccess
+               ? FOS_OK
+               : FOS_ERR_CUDA;
+  if (a == nullptr || m == nullptr) return FOS_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(m) || !aligned16(out) || (d.ld_probs & 7) != 0)
+    return FOS_ERR_UNSUPPORTED;
+  if ((int64_t)d.batch * d.kv_heads > 65535) return FOS_ERR_UNSUPPORTED;
+  DevInfo *dev = nullptr;
+  fos_status st = device_info(&dev);
+  if (st != FOS_OK) return st;
+  return run_kvgrad(desc, in_dtype, out_dtype, a, m, out, stream, dev->err, dev->max_smem);
 }
 
 extern "C" fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *delta,

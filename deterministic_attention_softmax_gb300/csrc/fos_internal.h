@@ -192,6 +192,11 @@ fos_status run_qk(const fos_qk_desc *d, fos_dtype in_dt, fos_dtype out_dt, const
 size_t pv_smem_bytes(int head_dim);
 fos_status run_pv(const fos_pv_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *p,
                   const void *v, void *out, cudaStream_t stream, unsigned *err, int max_smem);
+// The key / value gradient contraction (fos_kvgrad.cu): out = scale * a^T m per key head, the
+// group's query heads and positions accumulated in order.
+size_t kvgrad_smem_bytes(int head_dim);
+fos_status run_kvgrad(const fos_pv_desc *d, fos_dtype in_dt, fos_dtype out_dt, const void *a,
+                      const void *m, void *out, cudaStream_t stream, unsigned *err, int max_smem);
 
 // Host-side checks shared by the C ABI entry points (fos_api.cu).
 int dtype_size(fos_dtype dt);

@@ -20,8 +20,9 @@
 // the 128-byte swizzle through a ring of stages.  Lane 0 of warp 0 issues the copies, lane 0 of
 // warp 1 the MMAs; each stage's MMAs are committed to that stage's "empty" mbarrier, which lets
 // the copies of a later block into it, and the last commit releases the epilogue.  Every wait is
-// bounded.  The epilogue is fos_qk.cu's: lanes of the accumulator to registers, one rounding,
-// 128-byte-swizzled staging, TMA tensor stores.
+// bounded.  The epilogue is fos_qk.cu's: lanes of the accumulator to registers, the scale (1
+// for P V, the score scale for dQ = scale * dScores K), one rounding, 128-byte-swizzled
+// staging, TMA tensor stores.
 #include "fos_device.cuh"
 #include "fos_internal.h"
 #include "fos_tc.cuh"
@@ -42,6 +43,7 @@ struct PvArgs {
   int32_t dblocks;         // head dimension / 64 (1 or 2)
   int32_t q_heads, group;  // query heads; query heads per key/value head
   int32_t kblocks;         // ceil(kv_len / 64)
+  float scale;             // multiplies the float32 sum (1 for P V: an exact no-op)
   uint64_t timeout_ns;
   unsigned *err;
 };
@@ -146,6 +148,8 @@ __global__ void __launch_bounds__(kPvThreads, 1)
       for (int h = 0; h < kCols / 32; ++h) {
         float v[32];
         tmem_ld32(trow + (uint32_t)(c * kCols + h * 32), v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __fmul_rn(v[q], a.scale);
         if constexpr (sizeof(OutT) == 4) {
 #pragma unroll
           for (int q = 0; q < 32; ++q) packed[q] = __float_as_uint(v[q]);
@@ -230,6 +234,7 @@ fos_status run_pv(const fos_pv_desc *d, fos_dtype in_dt, fos_dtype out_dt, const
   a.q_heads = d->q_heads;
   a.group = d->q_heads / d->kv_heads;
   a.kblocks = (d->kv_len + kPvKB - 1) / kPvKB;
+  a.scale = d->scale;
   a.timeout_ns = 2000000000ull;
   a.err = err;
   const uint32_t idesc = f16_idesc(in_dt == FOS_BF16, kPvBM, d->head_dim, true);

@@ -38,11 +38,14 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t mn_bl
 }
 
 // Instruction descriptor of kind::f16: float32 accumulator (bits 4-5 = 1), A and B of the
-// same 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), A K-major (bit 15 = 0), B K-major
-// (bit 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t f16_idesc(bool bf16, int m, int n, bool b_mn_major) {
+// same 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), A K-major (bit 15 = 0) or MN-major
+// (bit 15 = 1), B K-major (bit 16 = 0) or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t f16_idesc(bool bf16, int m, int n, bool b_mn_major,
+                                                 bool a_mn_major = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,

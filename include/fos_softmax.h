@@ -371,23 +371,26 @@ fos_status fos_qk_scores(const fos_qk_desc *desc, fos_dtype in_dtype, fos_dtype 
                          const void *q, const void *k, void *scores, cudaStream_t stream);
 
 /*
- * The PV contraction behind the softmax: out[b, h, i, d] = sum_j probs[b, h, i, j] *
+ * The PV contraction behind the softmax: out[b, h, i, d] = scale * sum_j probs[b, h, i, j] *
  * v[b, h / (q_heads / kv_heads), j, d] on the tensor cores, the keys accumulated in float32 in a
- * fixed order (steps of 16, ascending from key 0), rounded once to the output dtype.  Each
- * output depends only on its probability row and the value rows, so it has the same bits
- * whatever the batch, the heads around it or its row's position.  ("Batch-invariant attention
- * (standard softmax--cuda version)", Fixed Reduction Contract: one writer per output, the keys
- * in a fixed order; "[WS1][kernels] Add fixed-order joint-attention softmax for Qwen-Image",
- * Summary: the softmax feeds the AV GEMM.)
+ * fixed order (steps of 16, ascending from key 0), multiplied by scale (one rounding; scale 1 is
+ * an exact no-op) and rounded once to the output dtype.  With (probs, v, scale) = (dScores, K,
+ * the score scale) the same call gives the query gradient dQ.  Each output depends only on its
+ * probability row and the value rows, so it has the same bits whatever the batch, the heads
+ * around it or its row's position.  ("Batch-invariant attention (standard softmax--cuda
+ * version)", Fixed Reduction Contract: one writer per output, the keys in a fixed order;
+ * "[WS1][kernels] Add fixed-order joint-attention softmax for Qwen-Image", Summary: the softmax
+ * feeds the AV GEMM.)
  */
 typedef struct fos_pv_desc {
   int32_t batch;      /* B */
   int32_t q_heads;    /* Hq, a multiple of kv_heads */
   int32_t kv_heads;   /* Hkv >= 1; query head h reads value head h / (Hq / Hkv) */
   int32_t q_len;      /* Sq */
-  int32_t kv_len;     /* Skv >= 1 */
+  int32_t kv_len;     /* Skv (>= 1 for fos_pv_out) */
   int32_t head_dim;   /* D: 64 or 128 */
-  int64_t ld_probs;   /* elements between rows of probs, >= kv_len */
+  int64_t ld_probs;   /* elements between rows of probs (of `a` for fos_grad_kv), >= kv_len */
+  float scale;        /* finite and nonzero: 1 for P V */
 } fos_pv_desc;
 
 /*
@@ -398,14 +401,38 @@ typedef struct fos_pv_desc {
  *          dense; must not overlap probs or v
  * probs, v and out must start on 16-byte boundaries and ld_probs must be a multiple of 8
  * (FOS_ERR_UNSUPPORTED otherwise).  FOS_ERR_INVALID for a bad description (negative sizes,
- * kv_len < 1, q_heads not a multiple of kv_heads, ld_probs < kv_len) or dtype;
- * FOS_ERR_UNSUPPORTED for another head dimension or more than 65535 (batch x query heads).  A
- * problem with no output is a no-op.  Resources: each CTA allocates head_dim tensor-memory
- * columns and frees them before it exits; a bounded wait that runs out is reported by
- * fos_device_error() as FOS_ERR_TIMEOUT.
+ * kv_len < 1, q_heads not a multiple of kv_heads, ld_probs < kv_len, scale zero or not finite)
+ * or dtype; FOS_ERR_UNSUPPORTED for another head dimension or more than 65535 (batch x query
+ * heads).  A problem with no output is a no-op.  Resources: each CTA allocates head_dim
+ * tensor-memory columns and frees them before it exits; a bounded wait that runs out is
+ * reported by fos_device_error() as FOS_ERR_TIMEOUT.
  */
 fos_status fos_pv_out(const fos_pv_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
                       const void *probs, const void *v, void *out, cudaStream_t stream);
+
+/*
+ * The contraction behind the key and value gradients of attention:
+ *   out[b, g, j, d] = scale * sum over the query heads h = g*G .. g*G + G - 1 (G = q_heads /
+ *                     kv_heads, ascending) and the query positions i = 0 .. q_len - 1
+ *                     (ascending, in steps of 16) of a[b, h, i, j] * m[b, h, i, d],
+ * accumulated in float32 on the tensor cores, multiplied by scale (one rounding) and rounded once
+ * to the output dtype.  (a, m, scale) = (P, dO, 1) gives dV, (dScores, Q, the score scale) dK.
+ * Each output has one writer and depends only on its key's column of a and on m, so it has the
+ * same bits whatever the batch or its key's position.  ("Batch-invariant attention (standard
+ * softmax--cuda version)", GQA backward: each dK / dV element accumulates the group's query
+ * heads, then the query positions, in a fixed order, with no atomics.)
+ *   desc   as for fos_pv_out, ld_probs giving the row stride of a; kv_len >= 0
+ *   a      device [batch][q_heads][q_len][ld_probs] of in_dtype (FOS_BF16 or FOS_F16); columns
+ *          kv_len .. ld_probs-1 are not read
+ *   m      device [batch][q_heads][q_len][head_dim] of in_dtype, dense
+ *   out    device [batch][kv_heads][kv_len][head_dim] of out_dtype, dense; must not overlap a or m
+ * Alignment and errors as for fos_pv_out (more than 65535 (batch x kv_heads) is
+ * FOS_ERR_UNSUPPORTED).  q_len == 0 writes +0 to every output; a problem with no output is a
+ * no-op.  Resources: each CTA allocates head_dim tensor-memory columns and frees them before it
+ * exits; a bounded wait that runs out is reported by fos_device_error() as FOS_ERR_TIMEOUT.
+ */
+fos_status fos_grad_kv(const fos_pv_desc *desc, fos_dtype in_dtype, fos_dtype out_dtype,
+                       const void *a, const void *m, void *out, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reports and clears the device error word of the current

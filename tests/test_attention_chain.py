@@ -1,8 +1,9 @@
 """Deterministic attention end to end on the library's kernels: the QK scores (fos_qk_scores),
 the fixed-order softmax (fos_softmax_fwd, in place on the score rows) and the PV contraction
 (fos_pv_out), chained in one 16-bit dtype, against the FP64 oracle's attention on the same Q, K
-and V, within a bound derived from the chain's roundings; and the chain's bits for a batch entry
-embedded in a larger batch.  ("[WS1][kernels] Add fixed-order joint-attention softmax for
+and V, within a bound derived from the chain's roundings; the gradients dQ, dK, dV through the
+same kernels, the softmax backward and the key / value gradient contraction (fos_grad_kv)
+against the oracle's; and the chain's bits for a batch entry embedded in a larger batch.  ("[WS1][kernels] Add fixed-order joint-attention softmax for
 Qwen-Image", Summary: the QK GEMM -> softmax -> AV GEMM chain; "Batch-invariant attention
 (standard softmax--cuda version)", Fixed Reduction Contract.)
 
@@ -95,3 +96,85 @@ def test_attention_bits_do_not_depend_on_the_batch():
     torch.cuda.synchronize()
     assert fos.fos_device_error() == 0
     assert bits_equal(out[1:2].contiguous(), ref)
+
+
+def chain_backward(q, k, v, dout, scale):
+    """Forward as above, then dP = dO V^T (QK kernel), dS = P (dP - delta) in place of dP
+    (softmax backward), dQ = scale dS K (PV kernel), dK = scale dS^T Q and dV = P^T dO
+    (key / value gradient kernel): every step in the library."""
+    B, Hq, Sq, _ = q.shape
+    Hkv = k.shape[1]
+    s = fos.fos_qk_scores(q, k, scale, out_dtype=q.dtype)
+    fos.fos_softmax_fwd(s, s, batch=B, heads=Hq, q_len=Sq)  # P in place of the scores
+    dp = fos.fos_qk_scores(dout, v, 1.0, out_dtype=q.dtype)
+    fos.fos_softmax_bwd(s, dp, dp, batch=B, heads=Hq, q_len=Sq)  # dS in place of dP
+    dq = fos.fos_pv_out(dp, k, scale=scale)
+    dk = fos.fos_grad_kv(dp, q, Hkv, scale)
+    dv = fos.fos_grad_kv(s, dout, Hkv)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("name", ["bfloat16", "float16"])
+@pytest.mark.parametrize("Hkv", [1, 2, 4])
+def test_attention_gradients_match_the_oracle(name, Hkv):
+    # The oracle's FP64 gradients of the same attention (its softmax VJP and the contractions'
+    # gradients), against a bound carried through the chain's roundings (first order, with a
+    # factor 1.5): P as in the forward bound (relative eps_i per row); dP rounded once after a
+    # float32 dot product (u |dP| + 2^-16 sum |dO v|); delta summed in float32 from both; dS
+    # rounded once; then the float32 contractions of dS (2^-16 of their absolute sums).
+    B, Hq, Sq, Skv, D = 2, 4, 200, 300, 128
+    dt = DTYPES[name]
+    q, k, v = inputs(B, Hq, Hkv, Sq, Skv, D, dt, seed=Hkv + 71)
+    g = torch.Generator(device="cuda").manual_seed(Hkv + 72)
+    dout = torch.randn(B, Hq, Sq, D, generator=g, device=dev()).to(dt)
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = chain_backward(q, k, v, dout, scale)
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+
+    qn, kn, vn, don = np64(q), np64(k), np64(v), np64(dout)
+    s, absqk, p, _, _ = reference(q, k, v, scale)
+    dp, dv_ref = gemm.pv_backward(don, p, vn)
+    ds, delta = oracle.softmax_bwd(p.reshape(-1, Skv), dp.reshape(-1, Skv), batch=B, heads=Hq,
+                                   q_len=Sq)
+    ds, delta = ds.reshape(p.shape), delta.reshape(p.shape[:-1] + (1,))
+    dq_ref, dk_ref = gemm.qk_backward(ds, qn, kn, scale)
+
+    u = UNIT_ROUNDOFF[name]
+    sub = SUBNORMAL_HALF_SPACING[name]
+    eps = 1.25 * (u + 2.0 * (u * np.abs(s) + 2.0 ** -16 * scale * absqk).max(-1, keepdims=True))
+    dp_abs = gemm.pv_backward(np.abs(don), p, np.abs(vn))[0]  # sum_d |dO_d v_jd|
+    e_dp = u * np.abs(dp) + 2.0 ** -16 * dp_abs
+    e_p = eps * p + sub
+    e_delta = (e_p * np.abs(dp) + p * e_dp).sum(-1, keepdims=True) + \
+        2.0 ** -20 * (p * np.abs(dp)).sum(-1, keepdims=True)
+    e_ds = e_p * np.abs(dp - delta) + p * (e_dp + e_delta) + u * np.abs(ds) + sub
+    zkv = np.zeros_like(kn)
+    # dQ = scale dS K, dK = scale sum_h dS^T Q: error of dS carried through, plus float32 sums
+    bq, bk = gemm.qk_backward(e_ds, np.abs(qn), np.abs(kn), scale)
+    aq, ak = gemm.qk_backward(np.abs(ds), np.abs(qn), np.abs(kn), scale)
+    bound_dq = 1.5 * (bq + 2.0 ** -16 * aq) + 1e-30
+    bound_dk = 1.5 * (bk + 2.0 ** -16 * ak) + 1e-30
+    # dV = sum_h P^T dO: the error of P carried through, plus the float32 sum
+    _, bv = gemm.pv_backward(np.abs(don), e_p + 2.0 ** -16 * p, zkv)
+    bound_dv = 1.5 * bv + 1e-30
+    for got, ref, bound, what in ((dq, dq_ref, bound_dq, "dQ"), (dk, dk_ref, bound_dk, "dK"),
+                                  (dv, dv_ref, bound_dv, "dV")):
+        worst = float((np.abs(np64(got) - ref) / bound).max())
+        assert worst <= 1.0, f"{what}: worst err/bound {worst:.3g}"
+
+
+def test_attention_gradient_bits_do_not_depend_on_the_batch():
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 150, 260, 128
+    q, k, v = inputs(B, Hq, Hkv, Sq, Skv, D, torch.bfloat16, seed=81)
+    g = torch.Generator(device="cuda").manual_seed(82)
+    dout = torch.randn(B, Hq, Sq, D, generator=g, device=dev()).to(torch.bfloat16)
+    ref = chain_backward(q, k, v, dout, 0.09)
+    q3, k3, v3 = inputs(3, Hq, Hkv, Sq, Skv, D, torch.bfloat16, seed=83)
+    d3 = torch.randn(3, Hq, Sq, D, generator=g, device=dev()).to(torch.bfloat16)
+    q3[1], k3[1], v3[1], d3[1] = q[0], k[0], v[0], dout[0]
+    out = chain_backward(q3, k3, v3, d3, 0.09)
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+    for a, b in zip(out, ref):
+        assert bits_equal(a[1:2].contiguous(), b)
