@@ -10,7 +10,8 @@ the same kernels as a differentiable op.
 """
 
 from ._build import build
-from .autograd import FixedOrderSoftmax, fixed_order_softmax
+from .autograd import (FixedOrderAttention, FixedOrderSoftmax, fixed_order_attention,
+                       fixed_order_softmax)
 from .binding import (FosError, Launch, fos_contract_fingerprint, fos_device_error,
                       fos_grad_kv, fos_pv_out, fos_qk_scores, fos_sink_grad, fos_sink_grad_merge,
                       fos_sink_grad_partials, fos_softmax_bwd, fos_softmax_bwd_sink,
@@ -18,7 +19,8 @@ from .binding import (FosError, Launch, fos_contract_fingerprint, fos_device_err
                       fos_step_host_workspace_bytes, sink_chunk_range)
 
 __all__ = [
-    "FixedOrderSoftmax", "FosError", "Launch", "build", "fixed_order_softmax",
+    "FixedOrderAttention", "FixedOrderSoftmax", "FosError", "Launch", "build",
+    "fixed_order_attention", "fixed_order_softmax",
     "fos_contract_fingerprint", "fos_device_error", "fos_grad_kv", "fos_pv_out", "fos_qk_scores",
     "fos_sink_grad", "fos_sink_grad_merge", "fos_sink_grad_partials", "fos_softmax_bwd",
     "fos_softmax_bwd_sink", "fos_softmax_fwd", "fos_softmax_step_host", "fos_status_string",

@@ -1,4 +1,5 @@
-"""``torch.autograd`` over the library's kernels: the fixed-order softmax as a differentiable op.
+"""``torch.autograd`` over the library's kernels: the fixed-order softmax, and attention built
+on it, as differentiable ops.
 
 ``fixed_order_softmax(scores, ...)`` returns ``(P, LSE)``.  Its backward maps dP to dScores
 with ``fos_softmax_bwd``: the VJP on the stored P, dScores_j = P_j * (dP_j - delta).  When the
@@ -65,3 +66,55 @@ def fixed_order_softmax(scores, *, batch=None, heads=None, q_len=None, causal=Fa
     _, _, _, batch, heads, q_len = binding._geometry(scores, batch, heads, q_len)
     return FixedOrderSoftmax.apply(scores, sink, batch, heads, q_len, bool(causal),
                                    kv_valid_len, key_mask)
+
+
+class FixedOrderAttention(torch.autograd.Function):
+    """out = softmax(scale Q K^T) V per (batch, query head) (see ``fixed_order_attention``)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale):
+        B, Hq, Sq, _ = q.shape
+        s = binding.fos_qk_scores(q, k, scale, out_dtype=q.dtype)
+        binding.fos_softmax_fwd(s, s, batch=B, heads=Hq, q_len=Sq)  # P in place of the scores
+        out = binding.fos_pv_out(s, v, out_dtype=q.dtype)
+        ctx.save_for_backward(q, k, v, s)
+        ctx.scale = scale
+        return out
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, dout):
+        q, k, v, p = ctx.saved_tensors
+        B, Hq, Sq, _ = q.shape
+        if dout.dtype != q.dtype or not dout.is_contiguous():
+            dout = dout.to(q.dtype).contiguous()  # the kernels take one dense 16-bit layout
+        dp = binding.fos_qk_scores(dout, v, 1.0, out_dtype=q.dtype)  # dP = dO V^T
+        binding.fos_softmax_bwd(p, dp, dp, batch=B, heads=Hq, q_len=Sq,
+                                want_delta=False)  # dS in place of dP
+        need_q, need_k, need_v = ctx.needs_input_grad[:3]
+        dq = binding.fos_pv_out(dp, k, scale=ctx.scale, out_dtype=q.dtype) if need_q else None
+        dk = binding.fos_grad_kv(dp, q, k.shape[1], ctx.scale, out_dtype=k.dtype) \
+            if need_k else None
+        dv = binding.fos_grad_kv(p, dout, k.shape[1], 1.0, out_dtype=v.dtype) if need_v else None
+        return dq, dk, dv, None
+
+
+def fixed_order_attention(q, k, v, scale=None):
+    """Differentiable attention on the library's kernels: scores = scale Q K^T (``fos_qk_scores``),
+    P = the fixed-order softmax of each score row (``fos_softmax_fwd``, in place), out = P V
+    (``fos_pv_out``); the backward is dP = dO V^T, dS = the softmax VJP, dQ = scale dS K,
+    dK = scale dS^T Q and dV = P^T dO (``fos_grad_kv``), the group's query heads and positions
+    in a fixed order ("Batch-invariant attention (standard softmax--cuda version)", Fixed
+    Reduction Contract and GQA backward).
+
+    ``q``: CUDA ``[batch, q_heads, q_len, D]``, ``k`` and ``v``: ``[batch, kv_heads, kv_len,
+    D]``, all dense bf16 or all dense fp16, D = 64 or 128, q_heads a multiple of kv_heads.
+    ``scale`` defaults to 1 / sqrt(D).  The output and the gradients have the inputs' dtype,
+    each rounded once from float32.
+    """
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k and v must be CUDA tensors")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Hq, Sq, D], k and v [B, Hkv, Skv, D]")
+    scale = q.shape[-1] ** -0.5 if scale is None else float(scale)
+    return FixedOrderAttention.apply(q.contiguous(), k.contiguous(), v.contiguous(), scale)

@@ -72,3 +72,42 @@ def test_only_what_is_asked_for():
     p, _ = fos.fixed_order_softmax(x, sink=c["sink"], batch=1, heads=2, q_len=4)
     p.backward(c["dp"].float().to(torch.bfloat16))
     assert x.grad is not None and x.grad.dtype == torch.bfloat16
+
+
+def test_attention_refuses_cpu_tensors():
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, requires_grad=True)
+    k = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fos.fixed_order_attention(q, k, k)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_attention_gradients_are_the_direct_calls_bits(dtype, Hkv):
+    # fixed_order_attention's output and its dQ, dK, dV against the same library calls made
+    # directly (QK, softmax in place, PV; dP by QK, dS in place, dQ by PV with the scale, dK and
+    # dV by the key / value gradient kernel), bit for bit
+    B, Hq, Sq, Skv, D = 2, 4, 130, 200, 64
+    g = torch.Generator(device="cuda").manual_seed(Hkv + 90)
+    q = torch.randn(B, Hq, Sq, D, generator=g, device="cuda").to(dtype)
+    k = torch.randn(B, Hkv, Skv, D, generator=g, device="cuda").to(dtype)
+    v = torch.randn(B, Hkv, Skv, D, generator=g, device="cuda").to(dtype)
+    dout = torch.randn(B, Hq, Sq, D, generator=g, device="cuda").to(dtype)
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = fos.fixed_order_attention(qa, ka, va)
+    out.backward(dout)
+    scale = D ** -0.5
+    s = fos.fos_qk_scores(q, k, scale, out_dtype=dtype)
+    fos.fos_softmax_fwd(s, s, batch=B, heads=Hq, q_len=Sq)
+    o_ref = fos.fos_pv_out(s, v, out_dtype=dtype)
+    dp = fos.fos_qk_scores(dout, v, 1.0, out_dtype=dtype)
+    fos.fos_softmax_bwd(s, dp, dp, batch=B, heads=Hq, q_len=Sq, want_delta=False)
+    dq = fos.fos_pv_out(dp, k, scale=scale, out_dtype=dtype)
+    dk = fos.fos_grad_kv(dp, q, Hkv, scale, out_dtype=dtype)
+    dv = fos.fos_grad_kv(s, dout, Hkv, out_dtype=dtype)
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+    assert bits_equal(out.detach(), o_ref)
+    for got, ref in ((qa.grad, dq), (ka.grad, dk), (va.grad, dv)):
+        assert got.dtype == dtype and bits_equal(got, ref)
