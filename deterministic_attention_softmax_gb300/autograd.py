@@ -72,34 +72,35 @@ class FixedOrderAttention(torch.autograd.Function):
     """out = softmax(scale Q K^T) V per (batch, query head) (see ``fixed_order_attention``)."""
 
     @staticmethod
-    def forward(ctx, q, k, v, scale):
+    def forward(ctx, q, k, v, scale, causal, kv_valid_len):
         B, Hq, Sq, _ = q.shape
+        masks = dict(batch=B, heads=Hq, q_len=Sq, causal=causal, kv_valid_len=kv_valid_len)
         s = binding.fos_qk_scores(q, k, scale, out_dtype=q.dtype)
-        binding.fos_softmax_fwd(s, s, batch=B, heads=Hq, q_len=Sq)  # P in place of the scores
+        binding.fos_softmax_fwd(s, s, **masks)  # P in place of the scores; masked keys +0
         out = binding.fos_pv_out(s, v, out_dtype=q.dtype)
-        ctx.save_for_backward(q, k, v, s)
-        ctx.scale = scale
+        ctx.save_for_backward(q, k, v, s, kv_valid_len)
+        ctx.scale, ctx.causal = scale, causal
         return out
 
     @staticmethod
     @once_differentiable
     def backward(ctx, dout):
-        q, k, v, p = ctx.saved_tensors
+        q, k, v, p, kv_valid_len = ctx.saved_tensors
         B, Hq, Sq, _ = q.shape
+        masks = dict(batch=B, heads=Hq, q_len=Sq, causal=ctx.causal, kv_valid_len=kv_valid_len)
         if dout.dtype != q.dtype or not dout.is_contiguous():
             dout = dout.to(q.dtype).contiguous()  # the kernels take one dense 16-bit layout
         dp = binding.fos_qk_scores(dout, v, 1.0, out_dtype=q.dtype)  # dP = dO V^T
-        binding.fos_softmax_bwd(p, dp, dp, batch=B, heads=Hq, q_len=Sq,
-                                want_delta=False)  # dS in place of dP
+        binding.fos_softmax_bwd(p, dp, dp, want_delta=False, **masks)  # dS in place of dP
         need_q, need_k, need_v = ctx.needs_input_grad[:3]
         dq = binding.fos_pv_out(dp, k, scale=ctx.scale, out_dtype=q.dtype) if need_q else None
         dk = binding.fos_grad_kv(dp, q, k.shape[1], ctx.scale, out_dtype=k.dtype) \
             if need_k else None
         dv = binding.fos_grad_kv(p, dout, k.shape[1], 1.0, out_dtype=v.dtype) if need_v else None
-        return dq, dk, dv, None
+        return dq, dk, dv, None, None, None
 
 
-def fixed_order_attention(q, k, v, scale=None):
+def fixed_order_attention(q, k, v, scale=None, *, causal=False, kv_valid_len=None):
     """Differentiable attention on the library's kernels: scores = scale Q K^T (``fos_qk_scores``),
     P = the fixed-order softmax of each score row (``fos_softmax_fwd``, in place), out = P V
     (``fos_pv_out``); the backward is dP = dO V^T, dS = the softmax VJP, dQ = scale dS K,
@@ -109,12 +110,17 @@ def fixed_order_attention(q, k, v, scale=None):
 
     ``q``: CUDA ``[batch, q_heads, q_len, D]``, ``k`` and ``v``: ``[batch, kv_heads, kv_len,
     D]``, all dense bf16 or all dense fp16, D = 64 or 128, q_heads a multiple of kv_heads.
-    ``scale`` defaults to 1 / sqrt(D).  The output and the gradients have the inputs' dtype,
-    each rounded once from float32.
+    ``scale`` defaults to 1 / sqrt(D).  ``causal``: key j of query i is valid iff
+    j <= kv_len - q_len + i ("Batch-invariant attention", Prefill / Decode / KV-cache Contract:
+    one condition for full prefill, chunked prefill and decode); ``kv_valid_len``: optional
+    int32 ``[batch]``, keys j >= kv_valid_len[b] masked.  The softmax applies the masks (masked
+    P and dS are +0), so the contractions need none.  The output and the gradients have the
+    inputs' dtype, each rounded once from float32.
     """
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k and v must be CUDA tensors")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape != v.shape:
         raise ValueError("q must be [B, Hq, Sq, D], k and v [B, Hkv, Skv, D]")
     scale = q.shape[-1] ** -0.5 if scale is None else float(scale)
-    return FixedOrderAttention.apply(q.contiguous(), k.contiguous(), v.contiguous(), scale)
+    return FixedOrderAttention.apply(q.contiguous(), k.contiguous(), v.contiguous(), scale,
+                                     bool(causal), kv_valid_len)

@@ -53,15 +53,60 @@ def chain(q, k, v, scale):
     return fos.fos_pv_out(s, v)
 
 
-def reference(q, k, v, scale):
+def reference(q, k, v, scale, **masks):
     qn, kn, vn = np64(q), np64(k), np64(v)
     B, Hq, Sq, _ = qn.shape
     Skv = kn.shape[2]
     s = gemm.qk_scores(qn, kn, scale)
     absqk = gemm.qk_scores(np.abs(qn), np.abs(kn), 1.0)
-    p, _ = oracle.softmax_fwd(s.reshape(-1, Skv), batch=B, heads=Hq, q_len=Sq)
+    p, _ = oracle.softmax_fwd(s.reshape(-1, Skv), batch=B, heads=Hq, q_len=Sq, **masks)
     p = p.reshape(s.shape)
     return s, absqk, p, gemm.pv(p, vn), gemm.pv(p, np.abs(vn))
+
+
+def forward_bound(name, s, absqk, p, pv_abs, vn, scale):
+    """The forward's bound (module docstring) per output."""
+    u = UNIT_ROUNDOFF[name]
+    ds = u * np.abs(s) + 2.0 ** -16 * abs(scale) * absqk
+    coef = 1.25 * (u + 2.0 * ds.max(axis=-1, keepdims=True) + 2.0 ** -16)
+    v_abs_sum = gemm.pv(np.ones_like(p), np.abs(vn))  # sum_j |v_jd| per output
+    return coef * pv_abs + SUBNORMAL_HALF_SPACING[name] * v_abs_sum + 1e-30
+
+
+def gradient_references(name, q, k, v, dout, scale, **masks):
+    """The oracle's dQ, dK, dV and the bounds of the chain's roundings (see the gradient
+    test): (reference, bound) per gradient."""
+    B, Hq, Sq, _ = q.shape
+    Skv = k.shape[2]
+    qn, kn, vn, don = np64(q), np64(k), np64(v), np64(dout)
+    s, absqk, p, _, _ = reference(q, k, v, scale, **masks)
+    dp, dv_ref = gemm.pv_backward(don, p, vn)
+    ds, delta = oracle.softmax_bwd(p.reshape(-1, Skv), dp.reshape(-1, Skv), batch=B, heads=Hq,
+                                   q_len=Sq, **masks)
+    ds, delta = ds.reshape(p.shape), delta.reshape(p.shape[:-1] + (1,))
+    dq_ref, dk_ref = gemm.qk_backward(ds, qn, kn, scale)
+    u = UNIT_ROUNDOFF[name]
+    sub = SUBNORMAL_HALF_SPACING[name]
+    eps = 1.25 * (u + 2.0 * (u * np.abs(s) + 2.0 ** -16 * scale * absqk).max(-1, keepdims=True))
+    dp_abs = gemm.pv_backward(np.abs(don), p, np.abs(vn))[0]  # sum_d |dO_d v_jd|
+    e_dp = u * np.abs(dp) + 2.0 ** -16 * dp_abs
+    e_p = eps * p + sub
+    e_delta = (e_p * np.abs(dp) + p * e_dp).sum(-1, keepdims=True) + \
+        2.0 ** -20 * (p * np.abs(dp)).sum(-1, keepdims=True)
+    e_ds = e_p * np.abs(dp - delta) + p * (e_dp + e_delta) + u * np.abs(ds) + sub
+    # dQ = scale dS K, dK = scale sum_h dS^T Q: the error of dS carried through, plus the
+    # float32 sums; dV = sum_h P^T dO: the error of P carried through, plus the float32 sum
+    bq, bk = gemm.qk_backward(e_ds, np.abs(qn), np.abs(kn), scale)
+    aq, ak = gemm.qk_backward(np.abs(ds), np.abs(qn), np.abs(kn), scale)
+    _, bv = gemm.pv_backward(np.abs(don), e_p + 2.0 ** -16 * p, np.zeros_like(kn))
+    return ((dq_ref, 1.5 * (bq + 2.0 ** -16 * aq) + 1e-30),
+            (dk_ref, 1.5 * (bk + 2.0 ** -16 * ak) + 1e-30),
+            (dv_ref, 1.5 * bv + 1e-30))
+
+
+def assert_within(got, ref, bound, what):
+    worst = float((np.abs(np64(got) - ref) / bound).max())
+    assert worst <= 1.0, f"{what}: worst err/bound {worst:.3g}"
 
 
 @pytest.mark.parametrize("name", ["bfloat16", "float16"])
@@ -75,14 +120,7 @@ def test_attention_matches_the_oracle(name, D):
     torch.cuda.synchronize()
     assert fos.fos_device_error() == 0
     s, absqk, p, ref, pv_abs = reference(q, k, v, scale)
-    u = UNIT_ROUNDOFF[name]
-    ds = u * np.abs(s) + 2.0 ** -16 * abs(scale) * absqk
-    coef = 1.25 * (u + 2.0 * ds.max(axis=-1, keepdims=True) + 2.0 ** -16)
-    v_abs_sum = gemm.pv(np.ones_like(p), np.abs(np64(v)))  # sum_j |v_jd| per output
-    bound = coef * pv_abs + SUBNORMAL_HALF_SPACING[name] * v_abs_sum + 1e-30
-    err = np.abs(np64(out) - ref)
-    worst = float((err / bound).max())
-    assert worst <= 1.0, f"worst err/bound {worst:.3g}"
+    assert_within(out, ref, forward_bound(name, s, absqk, p, pv_abs, np64(v), scale), "out")
 
 
 def test_attention_bits_do_not_depend_on_the_batch():
@@ -132,36 +170,10 @@ def test_attention_gradients_match_the_oracle(name, Hkv):
     torch.cuda.synchronize()
     assert fos.fos_device_error() == 0
 
-    qn, kn, vn, don = np64(q), np64(k), np64(v), np64(dout)
-    s, absqk, p, _, _ = reference(q, k, v, scale)
-    dp, dv_ref = gemm.pv_backward(don, p, vn)
-    ds, delta = oracle.softmax_bwd(p.reshape(-1, Skv), dp.reshape(-1, Skv), batch=B, heads=Hq,
-                                   q_len=Sq)
-    ds, delta = ds.reshape(p.shape), delta.reshape(p.shape[:-1] + (1,))
-    dq_ref, dk_ref = gemm.qk_backward(ds, qn, kn, scale)
-
-    u = UNIT_ROUNDOFF[name]
-    sub = SUBNORMAL_HALF_SPACING[name]
-    eps = 1.25 * (u + 2.0 * (u * np.abs(s) + 2.0 ** -16 * scale * absqk).max(-1, keepdims=True))
-    dp_abs = gemm.pv_backward(np.abs(don), p, np.abs(vn))[0]  # sum_d |dO_d v_jd|
-    e_dp = u * np.abs(dp) + 2.0 ** -16 * dp_abs
-    e_p = eps * p + sub
-    e_delta = (e_p * np.abs(dp) + p * e_dp).sum(-1, keepdims=True) + \
-        2.0 ** -20 * (p * np.abs(dp)).sum(-1, keepdims=True)
-    e_ds = e_p * np.abs(dp - delta) + p * (e_dp + e_delta) + u * np.abs(ds) + sub
-    zkv = np.zeros_like(kn)
-    # dQ = scale dS K, dK = scale sum_h dS^T Q: error of dS carried through, plus float32 sums
-    bq, bk = gemm.qk_backward(e_ds, np.abs(qn), np.abs(kn), scale)
-    aq, ak = gemm.qk_backward(np.abs(ds), np.abs(qn), np.abs(kn), scale)
-    bound_dq = 1.5 * (bq + 2.0 ** -16 * aq) + 1e-30
-    bound_dk = 1.5 * (bk + 2.0 ** -16 * ak) + 1e-30
-    # dV = sum_h P^T dO: the error of P carried through, plus the float32 sum
-    _, bv = gemm.pv_backward(np.abs(don), e_p + 2.0 ** -16 * p, zkv)
-    bound_dv = 1.5 * bv + 1e-30
-    for got, ref, bound, what in ((dq, dq_ref, bound_dq, "dQ"), (dk, dk_ref, bound_dk, "dK"),
-                                  (dv, dv_ref, bound_dv, "dV")):
-        worst = float((np.abs(np64(got) - ref) / bound).max())
-        assert worst <= 1.0, f"{what}: worst err/bound {worst:.3g}"
+    for got, (ref, bound), what in zip((dq, dk, dv),
+                                       gradient_references(name, q, k, v, dout, scale),
+                                       ("dQ", "dK", "dV")):
+        assert_within(got, ref, bound, what)
 
 
 def test_attention_gradient_bits_do_not_depend_on_the_batch():
@@ -178,3 +190,50 @@ def test_attention_gradient_bits_do_not_depend_on_the_batch():
     assert fos.fos_device_error() == 0
     for a, b in zip(out, ref):
         assert bits_equal(a[1:2].contiguous(), b)
+
+
+@pytest.mark.parametrize("name", ["bfloat16", "float16"])
+def test_masked_attention_and_its_gradients_match_the_oracle(name):
+    # fixed_order_attention with the causal bound of a chunk (200 queries against 300 keys: key
+    # j of query i valid iff j <= 100 + i) and valid lengths (300 and 230 keys per batch entry):
+    # output and dQ, dK, dV against the oracle with the same masks, within the bounds above
+    B, Hq, Hkv, Sq, Skv, D = 2, 4, 2, 200, 300, 64
+    dt = DTYPES[name]
+    q, k, v = inputs(B, Hq, Hkv, Sq, Skv, D, dt, seed=91)
+    g = torch.Generator(device="cuda").manual_seed(92)
+    dout = torch.randn(B, Hq, Sq, D, generator=g, device=dev()).to(dt)
+    kv = torch.tensor([300, 230], dtype=torch.int32, device=dev())
+    scale = D ** -0.5
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = fos.fixed_order_attention(qa, ka, va, scale, causal=True, kv_valid_len=kv)
+    out.backward(dout)
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
+    masks = dict(causal=True, kv_valid_len=kv.cpu().numpy())
+    s, absqk, p, ref, pv_abs = reference(q, k, v, scale, **masks)
+    # the output is in the input dtype: one more rounding, u |ref|
+    bound = forward_bound(name, s, absqk, p, pv_abs, np64(v), scale) + \
+        UNIT_ROUNDOFF[name] * np.abs(ref)
+    assert_within(out.detach(), ref, bound, "out")
+    for got, (ref_g, bound_g), what in zip((qa.grad, ka.grad, va.grad),
+                                           gradient_references(name, q, k, v, dout, scale,
+                                                               **masks),
+                                           ("dQ", "dK", "dV")):
+        assert_within(got, ref_g, bound_g + UNIT_ROUNDOFF[name] * np.abs(ref_g), what)
+
+
+def test_chunked_prefill_and_decode_give_the_full_prefill_bits():
+    # The pages' prefill / decode contract: one causal condition (key j of query i valid iff
+    # j <= kv_len - q_len + i) for every mode.  Queries i0 .. i1 - 1 run against the first i1
+    # keys (a prefill chunk; one query for decode) give the bits of the same rows of the full
+    # causal prefill: a row's valid keys, tiles and key steps are the same, and the keys a
+    # longer cache adds enter as exact zeros.
+    B, Hq, Hkv, S, D = 1, 4, 2, 300, 128
+    q, k, v = inputs(B, Hq, Hkv, S, S, D, torch.bfloat16, seed=95)
+    full = fos.fixed_order_attention(q, k, v, causal=True)
+    for i0, i1 in ((0, 100), (100, 237), (237, 300), (150, 151), (299, 300)):
+        part = fos.fixed_order_attention(q[:, :, i0:i1], k[:, :, :i1], v[:, :, :i1],
+                                         causal=True)
+        assert bits_equal(part, full[:, :, i0:i1].contiguous()), (i0, i1)
+    torch.cuda.synchronize()
+    assert fos.fos_device_error() == 0
