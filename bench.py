@@ -52,7 +52,7 @@ def parse():
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
     ap.add_argument("--workload-iters", type=int, default=20)
     ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "qk_bf16", "pv",
-                                          "grad_kv"],
+                                          "grad_kv", "step"],
                     default=None,
                     help="profiling mode: one input set, `warmup` + `steps` launches of one "
                          "kernel, no other output (for ncu captures)")
@@ -950,6 +950,27 @@ def run_profile(args):
     kv = None if kv is None else kv.to(dev)
     geo = dict(batch=w.batch, heads=w.heads, q_len=w.q_len, causal=w.causal, kv_valid_len=kv)
     sink = None if not w.sink else W.sink_logits(w).to(dev)
+    if args.profile == "step":
+        # forward then backward on two alternating input sets, as in the timed loop; the
+        # `steps` steps after the warm-up form one profiler range (cudaProfilerStart / Stop)
+        sets = []
+        for i in range(2):
+            xs = W.scores(w, dev, seed_offset=1 + i)
+            sets.append((xs, torch.empty_like(xs), W.dprobs(w, dev, seed_offset=1 + i),
+                         torch.empty_like(xs), torch.empty(w.rows, device=dev),
+                         torch.empty(w.rows, device=dev)))
+        torch.cuda.synchronize()
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                torch.cuda.synchronize()
+                torch.cuda.profiler.start()
+            xs, ps, dps, dss, ls, ds_ = sets[i % 2]
+            fos.fos_softmax_fwd(xs, ps, ls, sink=sink, **geo)
+            fos.fos_softmax_bwd(ps, dps, dss, ds_, **geo)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        assert fos.fos_device_error() == 0
+        return
     x = W.scores(w, dev)
     p = torch.empty_like(x)
     lse = torch.empty(w.rows, dtype=torch.float32, device=dev)
