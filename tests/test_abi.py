@@ -47,6 +47,58 @@ def test_struct_layout_matches_the_header(abi):
     assert abi.FosLaunch.groups_per_cta.offset == 32
 
 
+def test_contraction_descriptors_match_the_header(abi):
+    # fos_pv_desc: 6 x int32, int64, float (padded to 8 bytes)
+    assert abi.FosPvDesc.ld_probs.offset == 24
+    assert abi.FosPvDesc.scale.offset == 32
+    assert ctypes.sizeof(abi.FosPvDesc) == 40
+
+
+def _pv(abi, **kw):
+    d = dict(batch=1, q_heads=2, kv_heads=1, q_len=8, kv_len=16, head_dim=64, ld_probs=16,
+             scale=1.0)
+    d.update(kw)
+    return abi.FosPvDesc(**d)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(scale=0.0), dict(scale=float("inf")), dict(scale=float("nan")),  # scale finite, nonzero
+    dict(q_heads=3, kv_heads=2),                                         # not a multiple of kv_heads
+    dict(kv_heads=0), dict(ld_probs=15), dict(batch=-1), dict(q_len=-1),
+])
+def test_contractions_reject_bad_descriptors(abi, bad):
+    lib = abi.lib()
+    d = _pv(abi, **bad)
+    assert lib.fos_pv_out(ctypes.byref(d), abi.FOS_BF16, abi.FOS_F32, FAKE, FAKE, FAKE,
+                          None) == abi.FOS_ERR_INVALID
+    assert lib.fos_grad_kv(ctypes.byref(d), abi.FOS_BF16, abi.FOS_F32, FAKE, FAKE, FAKE,
+                           None) == abi.FOS_ERR_INVALID
+
+
+def test_contractions_reject_bad_dtypes_and_pointers(abi):
+    lib = abi.lib()
+    d = _pv(abi)
+    # 16-bit inputs only; outputs float32, bf16 or fp16
+    assert lib.fos_grad_kv(ctypes.byref(d), abi.FOS_F32, abi.FOS_F32, FAKE, FAKE, FAKE,
+                           None) == abi.FOS_ERR_INVALID
+    assert lib.fos_grad_kv(ctypes.byref(d), abi.FOS_BF16, 7, FAKE, FAKE, FAKE,
+                           None) == abi.FOS_ERR_INVALID
+    assert lib.fos_grad_kv(None, abi.FOS_BF16, abi.FOS_F32, FAKE, FAKE, FAKE,
+                           None) == abi.FOS_ERR_INVALID
+    assert lib.fos_grad_kv(ctypes.byref(d), abi.FOS_BF16, abi.FOS_F32, None, FAKE, FAKE,
+                           None) == abi.FOS_ERR_INVALID
+    assert lib.fos_grad_kv(ctypes.byref(d), abi.FOS_BF16, abi.FOS_F32, FAKE, FAKE, None,
+                           None) == abi.FOS_ERR_INVALID
+    # another head dimension is valid but unsupported
+    d96 = _pv(abi, head_dim=96)
+    assert lib.fos_grad_kv(ctypes.byref(d96), abi.FOS_BF16, abi.FOS_F32, FAKE, FAKE, FAKE,
+                           None) == abi.FOS_ERR_UNSUPPORTED
+    # no output: a no-op, even with null pointers
+    d0 = _pv(abi, kv_len=0, ld_probs=0)
+    assert lib.fos_grad_kv(ctypes.byref(d0), abi.FOS_BF16, abi.FOS_F32, None, None, None,
+                           None) == abi.FOS_OK
+
+
 def test_status_strings_and_fingerprint(abi):
     lib = abi.lib()
     for code, name in abi.STATUS_NAMES.items():
