@@ -431,12 +431,22 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
                                       vp(d_sink.data_ptr()), vp(ws.data_ptr()),
                                       ws.numel(), sh, None), "bwd_sink")
 
+    fused_launch = _abi.FosLaunch(0, 0, 0, 0, 0, 0, 0, 0, 1)
+
+    def bwd_sink_fused():  # the same with the octets forced wherever a kernel takes them
+        call(lib.fos_softmax_bwd_sink(dref, dt, vp(p.data_ptr()), vp(dp.data_ptr()),
+                                      vp(ds.data_ptr()), None, vp(lse.data_ptr()),
+                                      vp(d_sink.data_ptr()), vp(ws.data_ptr()),
+                                      ws.numel(), sh, ctypes.byref(fused_launch)),
+             "bwd_sink_fused")
+
     fwd()
     ok, gate = parity_gate(fos, w, dev, x, dp, p, lse, kv, sink)
     if not ok:
         raise SystemExit(f"parity gate failed before timing on {w.name}: {gate}")
     kernels = [("fwd", fwd), ("bwd", bwd)] + ([("sink", sgrad)] if sink is not None else [])
-    extra = [("bwd_sink", bwd_sink)] if sink is not None else []
+    extra = [("bwd_sink", bwd_sink), ("bwd_sink_fused", bwd_sink_fused)] \
+        if sink is not None else []
     # L2 flush between launches: a READ of 512 MB (4x the L2), so that the timed kernel finds
     # only clean, unrelated lines in L2 (a write would leave dirty lines whose write-back the
     # next kernel would pay for)
@@ -469,6 +479,7 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
         raise SystemExit(f"device error while timing {w.name}")
     med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in cold.items()}
     fused = med.pop("bwd_sink", None)
+    forced = med.pop("bwd_sink_fused", None)
     step_ms = statistics.median(a.elapsed_time(b) for a, b in steps)
     vk = W.mean_valid_keys(w)
     b = W.algorithmic_bytes(w, valid_keys=vk)
@@ -490,7 +501,8 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
         "rows_per_s_fwd_bwd": w.rows / (cold_sum * 1e-3),
         "algorithmic_bytes": {k: b[k] for k in ("fwd", "bwd", "sink")},
         "input_sha256_first_1024_rows": sha256_rows(x, dp, rows=1024),
-        "bwd_with_sink_fused_cold_ms": fused,
+        "bwd_with_sink_cold_ms": fused,
+        "bwd_with_sink_octets_forced_cold_ms": forced,
         "bwd_then_sink_cold_ms": (med["bwd"] + med["sink"]) if fused is not None else None,
         "timing": f"medians of {iters} launches per kernel after {warmup} warm-up; cold = "
                   f"512 MB scratch read before each kernel; step = kernels back to back",

@@ -87,6 +87,7 @@ class FosLaunch(ctypes.Structure):
         ("test_stall", ctypes.c_int32),
         ("generic", ctypes.c_int32),
         ("groups_per_cta", ctypes.c_int32),
+        ("sink_fusion", ctypes.c_int32),
     ]
 
 

@@ -45,11 +45,12 @@ class Launch:
     test_stall: int = 0
     generic: int = 0  # 1: never the kernel specialised for the common case
     groups_per_cta: int = 0  # forward row groups per CTA (0: chosen by the library)
+    sink_fusion: int = 0  # fos_softmax_bwd_sink: 0 library's choice, 1 fuse where possible, 2 never
 
     def _c(self) -> _abi.FosLaunch:
         return _abi.FosLaunch(self.warps_per_cta, self.ctas, self.stages, self.load_path,
                               self.wait_timeout_ns, self.test_stall, self.generic,
-                              self.groups_per_cta)
+                              self.groups_per_cta, self.sink_fusion)
 
 
 def _rows_layout(t: torch.Tensor, name: str):

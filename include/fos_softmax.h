@@ -140,6 +140,10 @@ typedef struct fos_launch {
                             warps_per_cta warps per CTA, 1..15, each with its own ring of
                             `stages` rows; FOS_ERR_UNSUPPORTED where that kernel does not apply
                             (same bits) */
+  int32_t sink_fusion;    /* fos_softmax_bwd_sink only: 0 = the library's choice (the faster way
+                            measured), 1 = the backward takes the sink terms by octets wherever
+                            its kernel can, 2 = never (delta, then the sink-gradient kernel);
+                            the same bits every way */
 } fos_launch;
 
 /*
@@ -196,21 +200,22 @@ fos_status fos_sink_grad(const fos_desc *desc, const float *lse, const float *de
 
 /*
  * The backward and the sink gradient in one call: the results of fos_softmax_bwd followed by
- * fos_sink_grad, bit for bit.  Where the backward's kernels allow it (rows of at most 8 tiles,
- * and longer staged rows with at least four octets per CTA), they take the rows by octets, 8
- * consecutive positions (b, i) of one head, and write each octet's ascending float32 sum of
- * c_r = -(exp(sink_h - lse_r) * delta_r) to the workspace; a small kernel then combines them
- * per head by the sink gradient's own chunk tree and left-to-right order, so delta and LSE are
- * never read back and no atomic is used.  Otherwise (rows streamed in segments) the two
- * launches run.  ("[ROCm] Jax Add softmax sink (learnable off-by-one) support", Description and
- * review thread: d_sink reduced per head inside the backward; there by atomicAdd into a zeroed
- * buffer, here in a fixed order.)
+ * fos_sink_grad, bit for bit.  Staged rows of more than 8 tiles with at least four octets per
+ * CTA are taken by octets, 8 consecutive positions (b, i) of one head: the backward writes each
+ * octet's ascending float32 sum of c_r = -(exp(sink_h - lse_r) * delta_r) to the workspace and
+ * a small kernel combines them per head by the sink gradient's own chunk tree and left-to-right
+ * order, so delta and LSE are never read back and no atomic is used.  Otherwise the two
+ * launches run (delta to the workspace when none is given): for rows of at most 8 tiles they
+ * are the faster way (the one-warp kernel takes octets only when launch->sink_fusion is 1),
+ * and rows streamed in segments take no octets.  ("[ROCm] Jax Add softmax sink (learnable
+ * off-by-one) support", Description and review thread: d_sink reduced per head inside the
+ * backward; there by atomicAdd into a zeroed buffer, here in a fixed order.)
  *   desc->sink    required (FOS_ERR_INVALID otherwise)
  *   probs, dprobs, dscores, delta  as fos_softmax_bwd (delta may be NULL)
  *   lse           device float [rows] (input, as written by the forward)
  *   d_sink        device float [heads] (output)
  *   workspace     device, 16-byte aligned, at least fos_bwd_sink_workspace_bytes(desc) bytes
- *                 (the octet sums, or delta when none is given and the rows are streamed);
+ *                 (the octet sums, or delta when none is given and the octets are not taken);
  *                 owned by the caller, not to be touched until `stream` completes
  * heads == 0 is a no-op; rows == 0 writes d_sink = 0.
  */

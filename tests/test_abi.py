@@ -38,13 +38,13 @@ def test_library_exports_every_declared_symbol(abi):
 
 
 def test_struct_layout_matches_the_header(abi):
-    # fos_desc: 2 x int64, 6 x int32, 3 pointers; fos_launch: 4 x int32, int64, 3 x int32
-    # (padded to 8 bytes)
+    # fos_desc: 2 x int64, 6 x int32, 3 pointers; fos_launch: 4 x int32, int64, 4 x int32
     assert ctypes.sizeof(abi.FosDesc) == 64
     assert abi.FosDesc.kv_valid_len.offset == 40
     assert ctypes.sizeof(abi.FosLaunch) == 40
     assert abi.FosLaunch.wait_timeout_ns.offset == 16
     assert abi.FosLaunch.groups_per_cta.offset == 32
+    assert abi.FosLaunch.sink_fusion.offset == 36
 
 
 def test_contraction_descriptors_match_the_header(abi):
@@ -148,11 +148,11 @@ def test_rejects_null_pointers_and_bad_dtype(abi):
 @pytest.mark.parametrize("bad", [
     dict(warps_per_cta=17), dict(warps_per_cta=-1), dict(ctas=-2), dict(stages=17),
     dict(load_path=4), dict(wait_timeout_ns=-5), dict(test_stall=2), dict(generic=2),
-    dict(groups_per_cta=-1), dict(groups_per_cta=16),
+    dict(groups_per_cta=-1), dict(groups_per_cta=16), dict(sink_fusion=-1), dict(sink_fusion=3),
 ])
 def test_rejects_bad_launch_options(abi, bad):
     opts = dict(warps_per_cta=0, ctas=0, stages=0, load_path=0, wait_timeout_ns=0, test_stall=0,
-                generic=0, groups_per_cta=0)
+                generic=0, groups_per_cta=0, sink_fusion=0)
     opts.update(bad)
     lc = abi.FosLaunch(**opts)
     d = _desc(abi)

@@ -111,3 +111,34 @@ def test_attention_gradients_are_the_direct_calls_bits(dtype, Hkv):
     assert bits_equal(out.detach(), o_ref)
     for got, ref in ((qa.grad, dq), (ka.grad, dk), (va.grad, dv)):
         assert got.dtype == dtype and bits_equal(got, ref)
+
+
+CHILD_BACKWARD = """
+import torch
+import deterministic_attention_softmax_gb300 as fos
+g = torch.Generator(device="cuda").manual_seed(7)
+q = torch.randn(1, 2, 70, 64, generator=g, device="cuda").to(torch.bfloat16).requires_grad_()
+k = torch.randn(1, 1, 90, 64, generator=g, device="cuda").to(torch.bfloat16).requires_grad_()
+v = torch.randn(1, 1, 90, 64, generator=g, device="cuda").to(torch.bfloat16).requires_grad_()
+out = fos.fixed_order_attention(q, k, v, causal=True)
+out.backward(torch.ones_like(out))
+torch.cuda.synchronize()
+assert fos.fos_device_error() == 0
+print("ok", float(q.grad.float().abs().sum()), float(v.grad.float().abs().sum()))
+"""
+
+
+@pytest.mark.gpu
+def test_attention_backward_first_on_a_fresh_autograd_thread():
+    # In a fresh process the attention backward is the first library call on PyTorch's autograd
+    # worker thread, which has no CUDA context bound yet; the contractions' tensor maps need one
+    # (they are bound before encoding).  This failed with FOS_ERR_UNSUPPORTED before the fix.
+    import os
+    import subprocess
+    import sys
+
+    from conftest import ROOT
+
+    r = subprocess.run([sys.executable, "-c", CHILD_BACKWARD], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600, env=dict(os.environ))
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout + r.stderr[-3000:]

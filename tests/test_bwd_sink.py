@@ -1,8 +1,9 @@
 """The backward with the sink gradient taken along (fos_softmax_bwd_sink).  Its results must be
-the bits of fos_softmax_bwd followed by fos_sink_grad on every path: rows of at most 8 tiles
-(one warp per row, octets of positions per warp), longer staged rows (one CTA per row, octets
-per CTA when there are enough of them, else the two launches), rows streamed in segments and
-rows copied with plain loads.  Octets that straddle two batch entries (q_len not a multiple of
+the bits of fos_softmax_bwd followed by fos_sink_grad on every path and every strategy: rows of
+at most 8 tiles (one warp per row: the two launches by default, octets of positions per warp
+when the launch asks for them), longer staged rows (one CTA per row, octets per CTA when there
+are enough of them, else the two launches), rows streamed in segments and rows copied with plain
+loads.  Octets that straddle two batch entries (q_len not a multiple of
 8), fully masked rows, -inf sinks and a given or absent delta are covered; the sink workload's
 shape is also checked against the FP64 oracle end to end.  ("[ROCm] Jax Add softmax sink
 (learnable off-by-one) support", Description and review thread: d_sink reduced per head in the
@@ -56,13 +57,17 @@ def test_short_rows_one_warp_per_row(dt, L, causal):
     p, dp, lse, sink, kw = make(dt, 3, 5, 13, L, seed=L + causal, causal=causal,
                                 kv=[L, L // 3, L])
     compare(p, dp, lse, sink, kw)
-    for opts in (dict(warps_per_cta=1), dict(warps_per_cta=7, stages=2), dict(ctas=3)):
+    # the library's choice (two launches here), the octets forced, and never
+    for opts in (dict(warps_per_cta=1), dict(warps_per_cta=7, stages=2), dict(ctas=3),
+                 dict(sink_fusion=1), dict(sink_fusion=1, warps_per_cta=7, stages=2),
+                 dict(sink_fusion=1, ctas=3), dict(sink_fusion=2)):
         compare(p, dp, lse, sink, kw, launch=fos.Launch(**opts))
 
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("opts", [dict(ctas=16), dict(ctas=16, generic=1),
-                                  dict(ctas=12, warps_per_cta=3, stages=1), dict(), dict(generic=1)],
+                                  dict(ctas=12, warps_per_cta=3, stages=1), dict(), dict(generic=1),
+                                  dict(ctas=16, sink_fusion=2)],
                          ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "default")
 def test_longer_rows_one_cta_per_row(dt, opts):
     # 17-tile rows, 75 octets: on a grid of at most 18 CTAs every CTA takes octets; the
