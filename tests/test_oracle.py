@@ -212,6 +212,32 @@ def test_row_ids_select_the_same_rows():
     assert np.array_equal(p, full_p[ids]) and np.array_equal(lse, full_l[ids])
 
 
+def test_row_ids_past_2_31_find_their_batch_entry_and_position():
+    # A problem of 65536 x 4097 x 8 rows (more than 2^31): a row's batch entry and query
+    # position decide its mask, so each given row must equal the same query position of a
+    # one-entry, one-head problem with that entry's valid length, forward and backward.
+    B, H, Sq, L = 65536, 4097, 8, 8
+    rng = np.random.default_rng(8)
+    kv = rng.integers(0, L + 1, size=B).astype(np.int32)
+    base = (1 << 31) // Sq * Sq
+    ids = np.array([base - 1, base, base + 5, base + 8 * Sq + 7, B * H * Sq - 1], dtype=np.int64)
+    x = rng.normal(0, 2, size=(len(ids), L))
+    dp = rng.normal(0, 1, size=(len(ids), L))
+    geo = dict(batch=B, heads=H, q_len=Sq, causal=True, kv_valid_len=kv)
+    p, lse = oracle.softmax_fwd(x, row_ids=ids, **geo)
+    ds, delta = oracle.softmax_bwd(p, dp, row_ids=ids, **geo)
+    for k, r in enumerate(ids):
+        b, i = int(r) // (H * Sq), int(r) % Sq
+        one = dict(batch=1, heads=1, q_len=Sq, causal=True, kv_valid_len=kv[b:b + 1])
+        p1, l1 = oracle.softmax_fwd(x[k:k + 1], row_ids=[i], **one)
+        ds1, d1 = oracle.softmax_bwd(p1, dp[k:k + 1], row_ids=[i], **one)
+        assert np.array_equal(p[k], p1[0]) and np.array_equal(lse[k], l1[0], equal_nan=True)
+        assert np.array_equal(ds[k], ds1[0]) and np.array_equal(delta[k], d1[0])
+        # and the mask it applied is the definition's: causal bound and valid length
+        allowed = (np.arange(L) <= L - Sq + i) & (np.arange(L) < kv[b])
+        assert np.all(p[k][~allowed] == 0) and (not allowed.any() or np.all(p[k][allowed] > 0))
+
+
 # ----------------------------------------------------------------------------- brute force
 
 
