@@ -271,6 +271,49 @@ __device__ __forceinline__ void merge_tiles(int Te, int lane, const float *tm, c
   }
 }
 
+// merge_tiles for rows of at most 8 tiles (one warp per row): the same bits.  Lane t < 8 holds
+// tile t; its inclusive prefix maximum needs the shuffle distances 1, 2, 4 only (a lane below
+// the distance gets its own value back, which the maximum leaves unchanged).  The final maximum
+// is known once the prefix maxima are, so the numerators exp(m_t - M) of the scales are formed
+// beside the sequential fold, which then leaves only the division.
+__device__ __forceinline__ void merge_tiles8(int Te, int lane, const float *tm, const float *ts,
+                                             float *tc, float &M, float &S) {
+  if (Te <= 0) return;
+  const float mt = lane < Te ? tm[lane] : -INFINITY;
+  const float st = lane < Te ? ts[lane] : 0.0f;
+  float pm = mt;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) pm = fmaxf(pm, __shfl_up_sync(kFull, pm, o));
+  pm = fmaxf(pm, M);
+  float prev = __shfl_up_sync(kFull, pm, 1);
+  if (lane == 0) prev = M;
+  const float Mf = __shfl_sync(kFull, pm, Te - 1);
+  // flushing these factors cannot change S (see scale_ftz)
+  const float alpha = scale_ftz(prev, pm);
+  const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
+  const float num = scale_fos(mt, Mf);
+  float *ab = tc;  // scratch: the factors, read back by every lane (slots past Te: (1, 0))
+  if (lane < 8) {
+    ab[lane] = (lane < Te) ? alpha : 1.0f;
+    ab[32 + lane] = (lane < Te) ? beta : 0.0f;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q0 = 0; q0 < 8; q0 += 4) {
+    if (q0 < Te) {
+      const float4 av = *reinterpret_cast<const float4 *>(ab + q0);
+      const float4 bv = *reinterpret_cast<const float4 *>(ab + 32 + q0);
+      S = __fadd_rn(__fmul_rn(S, av.x), bv.x);
+      S = __fadd_rn(__fmul_rn(S, av.y), bv.y);
+      S = __fadd_rn(__fmul_rn(S, av.z), bv.z);
+      S = __fadd_rn(__fmul_rn(S, av.w), bv.w);
+    }
+  }
+  __syncwarp();
+  M = Mf;
+  if (lane < Te) tc[lane] = (mt == -INFINITY) ? 0.0f : __fdiv_rn(num, S);
+}
+
 // Copy keys [0, lim) of a row into the stage with plain loads (unaligned or forced path).
 template <typename T>
 __device__ __forceinline__ void plain_stage(unsigned char *stage, const unsigned char *src,
@@ -1074,11 +1117,15 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
       ok = false;
       break;
     }
+    // the head's sink logit, loaded now so that its latency passes under pass 1
+    const float sink_h = a.sink != nullptr ? a.sink[g.z] : -INFINITY;
+    // the rolled loops (KT = 8) stop after the row's last tile; the unrolled ones test each pair
+    const int kend = kPairUnroll == 1 ? Te : KT;
 
     // ---- pass 1: every tile of the row, two neighbouring tiles at a time
     float er0[8], er1[8];  // kRegs: the row's pair, kept for pass 2
 #pragma unroll(kPairUnroll)
-    for (int kk = 0; kk < KT; kk += 2) {
+    for (int kk = 0; kk < kend; kk += 2) {
       if constexpr (kRegs) {
         if (kk + 1 < Te)
           tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, er0, er1, tm, ts);
@@ -1108,10 +1155,10 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
     // ---- merge (this warp)
     float M = -INFINITY, S = 0.0f;
     if (a.sink != nullptr) {
-      M = a.sink[g.z];
+      M = sink_h;
       S = 1.0f;
     }
-    merge_tiles(Te, lane, tm, ts, tc, M, S);
+    merge_tiles8(Te, lane, tm, ts, tc, M, S);
     __syncwarp();  // tc
     if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
@@ -1130,7 +1177,7 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
       tmem_wait_st();
     }
 #pragma unroll(kPairUnroll)
-    for (int kk = 0; kk < (kRegs ? 0 : KT); kk += 2) {
+    for (int kk = 0; kk < (kRegs ? 0 : kend); kk += 2) {
       float e0[8], e1[8];
       if (kk + 1 < Te) {
         tmem_ld16(tw + kk * 8, e0, e1);
