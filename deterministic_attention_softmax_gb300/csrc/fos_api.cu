@@ -216,7 +216,8 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t 
                      const void *const *inputs, int copies,
                      const void *output, const fos_launch *l, const DevInfo &dev,
                      size_t (*extra)(int, int), int default_warps, size_t stage_target,
-                     uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl, int seg_tiles = 0) {
+                     uint32_t occ_key, OccFn occ, RowArgs *ra, Plan *pl, int seg_tiles = 0,
+                     int extra_warps = 1) {
   const int esz = dtype_size(dt);
   const int T = (d->key_len + kTileK - 1) / kTileK;
   const int stage_tiles = (seg_tiles > 0 && seg_tiles < T) ? seg_tiles : T;
@@ -232,7 +233,8 @@ fos_status plan_rows(const fos_desc *d, fos_dtype dt, int64_t row_base, int64_t 
   const bool bulk = need_bulk || (path == 0 && bulk_ok);
 
   const int warps = (l && l->warps_per_cta) ? l->warps_per_cta : default_warps;
-  const int threads = (warps + 1) * 32;  // the compute warps and one producer warp
+  // the compute warps, one producer warp (and the streaming forward's merge warp)
+  const int threads = (warps + extra_warps) * 32;
   const size_t slot = (size_t)copies * stage_bytes;
   const size_t fixed = extra(T, 0);
   if (fixed + slot > (size_t)dev.max_smem) return FOS_ERR_UNSUPPORTED;
@@ -540,13 +542,13 @@ fos_status run_fwd(const fos_desc *desc, fos_dtype dtype, int64_t row_base, int6
     auto plan = [&](int warps) {
       const int seg = stream_seg_tiles(warps);
       return plan_rows(desc, dtype, row_base, nrows, inputs, 1, probs, launch, *dev,
-                       fwd_extra_smem, warps,
+                       fwd_stream_extra_smem, warps,
                        stream_ring_target(seg, dtype, 1, kStreamStagesFwd),
                        0x300u | ((uint32_t)dtype << 4),
                        [dtype](int th, size_t sm, int *n) {
                          return fwd_stream_occupancy(dtype, th, sm, n);
                        },
-                       &a, &pl, seg);
+                       &a, &pl, seg, 2);
     };
     st = plan(given ? launch->warps_per_cta : kStreamWarpsFwd);
     if (st == FOS_ERR_UNSUPPORTED && !given) st = plan(kStreamWarpsNarrow);

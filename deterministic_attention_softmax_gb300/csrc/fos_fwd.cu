@@ -882,6 +882,99 @@ __device__ void fwd_stream_produce(const FwdArgs &a, int64_t r0, int64_t G, int6
       mbar_wait_bounded(smem_addr(&full[t]), (last_ph >> t) & 1u, a.timeout_ns);
 }
 
+// One chunk of at most 32 tiles of the fold, in order, continuing from the running (M, S):
+// lane t takes tile t of the chunk.  The steps are those of merge_tiles (prefix maxima from
+// the running maximum, the factors, the sequential fold), so folding a row chunk by chunk, at
+// any chunk boundaries, gives the bits of merge_tiles.  ab is a 64-float scratch.
+__device__ __forceinline__ void fold_chunk(const float *tmc, const float *tsc, int n, int lane,
+                                           float *ab, float &M, float &S) {
+  const float mt = lane < n ? tmc[lane] : -INFINITY;
+  const float st = lane < n ? tsc[lane] : 0.0f;
+  float pm = mt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) pm = fmaxf(pm, __shfl_up_sync(kFull, pm, o));
+  pm = fmaxf(pm, M);
+  float prev = __shfl_up_sync(kFull, pm, 1);
+  if (lane == 0) prev = M;
+  // flushing these factors cannot change S (see scale_ftz)
+  const float alpha = scale_ftz(prev, pm);
+  const float beta = (mt == -INFINITY) ? 0.0f : __fmul_rn(st, scale_ftz(mt, pm));
+  ab[lane] = (lane < n) ? alpha : 1.0f;
+  ab[32 + lane] = (lane < n) ? beta : 0.0f;
+  __syncwarp();
+  for (int q0 = 0; q0 < n; q0 += 4) {
+    const float4 av = *reinterpret_cast<const float4 *>(ab + q0);
+    const float4 bv = *reinterpret_cast<const float4 *>(ab + 32 + q0);
+    S = __fadd_rn(__fmul_rn(S, av.x), bv.x);
+    S = __fadd_rn(__fmul_rn(S, av.y), bv.y);
+    S = __fadd_rn(__fmul_rn(S, av.z), bv.z);
+    S = __fadd_rn(__fmul_rn(S, av.w), bv.w);
+  }
+  __syncwarp();
+  M = __shfl_sync(kFull, pm, n - 1);
+}
+
+// The merge warp: it follows the ring through the same segments as the compute warps.  For
+// each pass-1 segment it waits until every compute warp has written that segment's tile
+// statistics (the stage's "statistics" barrier), folds them into the running (M, S) and then
+// releases the stage (its arrival on "empty" is one of the nw + 1 the producer waits for, so the
+// ring never runs more than a ring ahead of the fold).  After the row's last segment it writes
+// the scales c_t and the LSE, and meets the compute warps at barrier 1; pass 2 takes no part of
+// it (warp 0 arrives for it on "empty"), and barrier 2 ends the row for both.  A wait that runs
+// out stops the warp: it says so at the next barrier, where the compute warps learn of it.
+template <typename T>
+__device__ void fwd_stream_merge(const FwdArgs &a, int64_t r0, int64_t G, int64_t nmine,
+                                 uint64_t *empty, uint64_t *stat, const int4 *geos,
+                                 const float *tm, const float *ts, float *tc, float *ab, int nsync) {
+  const int lane = threadIdx.x & 31;
+  const int NS = a.stages;
+  const int SEG = a.seg_tiles;
+  int s = 0;
+  uint32_t stat_ph = 0;  // per stage: parity of its next "statistics" phase
+  for (int64_t k = 0; k < nmine; ++k) {
+    const int64_t r = r0 + k * G;
+    bool bad = false;
+    int Te = 0, nseg = 1;
+    float M = -INFINITY, S = 0.0f;
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!mbar_wait_bounded(smem_addr(&stat[s]), (stat_ph >> s) & 1u, a.timeout_ns)) {
+        bad = true;
+        break;
+      }
+      stat_ph ^= 1u << s;
+      if (seg == 0) {
+        const int4 g = geos[s];
+        Te = (g.x + kTileK - 1) / kTileK;
+        nseg = Te > 0 ? (Te + SEG - 1) / SEG : 1;
+        if (a.sink != nullptr) {
+          M = a.sink[g.z];
+          S = 1.0f;
+        }
+      }
+      const int t0 = seg * SEG, nt = min(SEG, Te - t0);
+      for (int c0 = 0; c0 < nt; c0 += 32)
+        fold_chunk(tm + t0 + c0, ts + t0 + c0, min(32, nt - c0), lane, ab, M, S);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (++s == NS) s = 0;
+    }
+    if (!bad) {
+#pragma unroll 4
+      for (int t = lane; t < Te; t += 32) {
+        const float mt = tm[t];
+        tc[t] = (mt == -INFINITY) ? 0.0f : __fdiv_rn(scale_fos(mt, M), S);
+      }
+      if (lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
+    }
+    if (named_sync_or(1, nsync, bad)) {
+      if (lane == 0 && bad) raise_device_error(a.err, kDevErrTimeout);
+      return;
+    }
+    s = (int)((s + nseg) % NS);  // the row's pass-2 segments
+    if (named_sync_or(2, nsync, false)) return;
+  }
+}
+
 template <typename T>
 __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -894,10 +987,14 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
   float *tm = reinterpret_cast<float *>(ring + (size_t)a.stages * a.stage_bytes);
   float *ts = tm + T4;
   float *tc = ts + T4;
+  // after tc (and the 16 bytes kept for a tensor-memory address by the other kernels' layout):
+  // the stages' "statistics" barriers, then the merge warp's fold scratch
+  uint64_t *stat = reinterpret_cast<uint64_t *>(tc + (T4 > 64 ? T4 : 64) + 4);
+  float *ab = reinterpret_cast<float *>(stat + 16);
 
   const int tid = threadIdx.x;
-  const int nw = (blockDim.x >> 5) - 1;  // compute warps; the last warp is the producer
-  const int ncomp = nw * 32;
+  const int nw = (blockDim.x >> 5) - 2;  // compute warps; then the merge warp and the producer
+  const int nsync = (nw + 1) * 32;       // compute warps and the merge warp
   const int w = tid >> 5;
   const int lane = tid & 31;
   const int64_t G = gridDim.x;
@@ -910,15 +1007,20 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
   if (tid == 0) {
     for (int t = 0; t < NS; ++t) {
       mbar_init(smem_addr(&full[t]), 1);
-      mbar_init(smem_addr(&empty[t]), nw);
+      mbar_init(smem_addr(&empty[t]), nw + 1);
+      mbar_init(smem_addr(&stat[t]), nw);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  if (w == nw) {
+  if (w == nw + 1) {
     if (lane == 0)
       fwd_stream_produce<T>(a, r0, G, nmine, full, empty, geos, ring,
                             a.test_stall && blockIdx.x == 0);
+    return;
+  }
+  if (w == nw) {
+    fwd_stream_merge<T>(a, r0, G, nmine, empty, stat, geos, tm, ts, tc, ab, nsync);
     return;
   }
 
@@ -931,7 +1033,7 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
     int lim = 0, Te = 0, nseg = 1;
     const uint8_t *km = nullptr;
 
-    // ---- pass 1: tile statistics, segment by segment
+    // ---- pass 1: tile statistics, segment by segment; the merge warp folds them behind
     for (int seg = 0; seg < nseg; ++seg) {
       if (!mbar_wait_bounded(smem_addr(&full[s]), ph, a.timeout_ns)) {
         timed_out = true;
@@ -959,29 +1061,22 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
         float e0[8];
         tile_stats1<T>(stage, tl, lane, lim_l, kms, e0, tm + t0, ts + t0);
       }
+      if (timed_out) break;  // (index check failed) its statistics are not announced
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&stat[s]));  // release: this warp's tm / ts entries
+        mbar_arrive(smem_addr(&empty[s]));
+      }
       if (++s == NS) {
         s = 0;
         ph ^= 1u;
       }
     }
-    if (compute_sync_or(ncomp, timed_out)) {
+    // the merge warp has folded the row and written tc and the LSE
+    if (named_sync_or(1, nsync, timed_out)) {
       if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
       return;
     }
-
-    // ---- merge (warp 0)
-    float M = -INFINITY, S = 0.0f;
-    if (w == 0) {
-      if (a.sink != nullptr) {
-        M = a.sink[g.z];
-        S = 1.0f;
-      }
-      merge_tiles(Te, lane, tm, ts, tc, M, S);
-    }
-    compute_sync(ncomp);
-    if (w == 0 && lane == 0) a.lse[r] = (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
 
     // ---- pass 2: every segment again, e_j recomputed, P written
     unsigned char *prow = static_cast<unsigned char *>(a.probs) + (size_t)r * a.ld * esz;
@@ -1001,7 +1096,10 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
         tile_store<T>(prow, t0 + tl, lane, a.L, ovec, ee, tc[t0 + tl]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&empty[s]));
+        if (w == 0) mbar_arrive(smem_addr(&empty[s]));  // the merge warp's share in pass 2
+      }
       if (++s == NS) {
         s = 0;
         ph ^= 1u;
@@ -1013,13 +1111,14 @@ __global__ void __maxnreg__(64) fos_fwd_stream_kernel(const FwdArgs a) {
       for (int q = 0; q < kLaneKeys; ++q) z[q] = 0.0f;
       store_lane8<T>(prow, t * kTileK + lane * kLaneKeys, a.L, ovec, z);
     }
-    // a wait that ran out in pass 2 stops every compute warp (none is left at a barrier)
-    if (compute_sync_or(ncomp, timed_out)) {
+    // a wait that ran out in pass 2 stops every compute warp and the merge warp
+    if (named_sync_or(2, nsync, timed_out)) {
       if (tid == 0) raise_device_error(a.err, kDevErrTimeout);
       return;
     }
-    // Each warp writes (pass 1) and reads (pass 2) the tm entries of its own tiles only, and tc
-    // is rewritten after the next row's first barrier.
+    // Each warp writes (pass 1) and reads (pass 2) the tm entries of its own tiles only; the
+    // merge warp reads a segment's entries once its warps have announced them, and tc is
+    // rewritten after the next row's pass 1.
   }
 }
 
@@ -1288,6 +1387,11 @@ size_t fwd_extra_smem(int T, int stages) {
   // (and 16 bytes for the tensor-memory address)
   return (size_t)kBarBytes + kGeoBytes + (size_t)(2 * T4 + (T4 > 64 ? T4 : 64)) * sizeof(float) +
          16;
+}
+
+size_t fwd_stream_extra_smem(int T, int stages) {
+  // fwd_extra_smem's layout, then 16 "statistics" mbarriers and the merge warp's 64-float scratch
+  return fwd_extra_smem(T, stages) + 16 * sizeof(uint64_t) + 64 * sizeof(float);
 }
 
 uint32_t fwd_tmem_cols(int warps, int kt) {

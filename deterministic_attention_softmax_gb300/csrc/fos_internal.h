@@ -123,6 +123,7 @@ inline void fill_sink_args(const fos_desc *d, SinkArgs *a) {
 
 // Shared memory used by a row kernel besides its ring of staged rows.
 size_t fwd_extra_smem(int T, int stages);
+size_t fwd_stream_extra_smem(int T, int stages);  // the streaming forward (merge warp)
 size_t bwd_extra_smem(int T, int stages);
 
 // Kernel instances per dtype: set the dynamic shared-memory limit, query residency, launch.
