@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload table (all synthetic workloads, cold medians)")
-    ap.add_argument("--workload-iters", type=int, default=20)
+    ap.add_argument("--workload-iters", type=int, default=50,
+                    help="timed launches per kernel in the per-workload table (after 10 warm-up)")
     ap.add_argument("--profile", choices=["fwd", "bwd", "sink", "bwd_sink", "qk", "qk_bf16", "pv",
                                           "grad_kv", "step"],
                     default=None,
@@ -371,7 +372,7 @@ def parity_gate(fos, w, dev, x, dp, p, lse, kv, sink, nrows=32):
     return ok, detail
 
 
-def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
+def measure_workload(fos, w, dev, peak, iters=50, warmup=10):
     """One workload: inputs resident in HBM, a parity gate, then per-kernel CUDA-event medians.
     `cold`: a 512 MB scratch read (4x the L2) before each kernel, so every kernel reads its
     inputs from DRAM and finds no dirty line of another kernel in L2 (its own writes still
@@ -517,7 +518,7 @@ def measure_workload(fos, w, dev, peak, iters=20, warmup=3):
     return out
 
 
-def measure_qk(fos, dev, hbm_peak, iters=20, warmup=3):
+def measure_qk(fos, dev, hbm_peak, iters=50, warmup=10):
     """The QK contraction that produces the benchmark's scores: 16,384 query rows (4 heads x
     4,096) against 4,352 keys, head dimension 128, bf16 Q and K, float32 and bf16 scores.  A
     parity gate on sampled query rows, then cold CUDA-event medians (512 MB scratch read before
