@@ -1221,10 +1221,12 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
     // the rolled loops (KT = 8) stop after the row's last tile; the unrolled ones test each pair
     const int kend = kPairUnroll == 1 ? Te : KT;
 
-    // ---- pass 1: every tile of the row, two neighbouring tiles at a time
+    // ---- pass 1: every tile of the row, two neighbouring tiles at a time (the lane's key
+    // pointer steps by two tiles)
     float er0[8], er1[8];  // kRegs: the row's pair, kept for pass 2
+    const unsigned char *sp = stage + (size_t)(lane * kLaneKeys) * esz;
 #pragma unroll(kPairUnroll)
-    for (int kk = 0; kk < kend; kk += 2) {
+    for (int kk = 0; kk < kend; kk += 2, sp += 2 * kTileK * esz) {
       if constexpr (kRegs) {
         if (kk + 1 < Te)
           tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, er0, er1, tm, ts);
@@ -1233,12 +1235,12 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
       } else {
         float e0[8], e1[8];
         if (kk + 1 < Te) {
-          tile_stats2<T>(stage, kk, kk + 1, lane, lim, km, e0, e1, tm, ts);
+          tile_stats2p<T>(sp, sp + kTileK * esz, kk, lane, lim, km, e0, e1, tm, ts);
           __syncwarp();
           tmem_st8(tw + kk * 8, e0);
           tmem_st8(tw + kk * 8 + 8, e1);
         } else if (kk < Te) {
-          tile_stats1<T>(stage, kk, lane, lim, km, e0, tm, ts);
+          tile_stats1p<T>(sp, kk, lane, lim, km, e0, tm, ts);
           __syncwarp();
           tmem_st8(tw + kk * 8, e0);
         }
@@ -1275,13 +1277,19 @@ __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdA
       __syncwarp();
       tmem_wait_st();
     }
+    unsigned char *pp = prow + (size_t)(lane * kLaneKeys) * esz;
 #pragma unroll(kPairUnroll)
-    for (int kk = 0; kk < (kRegs ? 0 : kend); kk += 2) {
+    for (int kk = 0; kk < (kRegs ? 0 : kend); kk += 2, pp += 2 * kTileK * esz) {
       float e0[8], e1[8];
       if (kk + 1 < Te) {
         tmem_ld16(tw + kk * 8, e0, e1);
-        tile_store<T>(prow, kk, lane, a.L, ovec, e0, tc[kk]);
-        tile_store<T>(prow, kk + 1, lane, a.L, ovec, e1, tc[kk + 1]);
+        if (ovec && (kk + 2) * kTileK <= a.L) {  // both tiles whole in the row: no key checks
+          tile_store_full<T>(pp, e0, tc[kk]);
+          tile_store_full<T>(pp + kTileK * esz, e1, tc[kk + 1]);
+        } else {
+          tile_store<T>(prow, kk, lane, a.L, ovec, e0, tc[kk]);
+          tile_store<T>(prow, kk + 1, lane, a.L, ovec, e1, tc[kk + 1]);
+        }
       } else if (kk < Te) {
         tmem_ld8(tw + kk * 8, e0);
         tile_store<T>(prow, kk, lane, a.L, ovec, e0, tc[kk]);
