@@ -825,10 +825,11 @@ __global__ void __maxnreg__(64) fos_fwd_group_kernel(const FwdArgs a) {
 //
 // A row whose staged copy would not fit in shared memory is read twice, in segments of
 // a.seg_tiles tiles that cycle through the same ring: pass 1 takes the tile statistics
-// segment by segment, the merge is the one above, and pass 2 reads every segment again and
-// recomputes e_j from the stored tile maxima, as the staged kernel's recompute mode does.  The
-// per-tile arithmetic and the merge are those of fos_fwd_kernel, so a row gives the same bits
-// on either path; the price is a second read of the scores.
+// segment by segment while a merge warp folds them behind it (the steps of merge_tiles, chunk
+// by chunk), and pass 2 reads every segment again and recomputes e_j from the stored tile
+// maxima, as the staged kernel's recompute mode does.  The per-tile arithmetic and the fold are
+// those of fos_fwd_kernel, so a row gives the same bits on either path; the price is a second
+// read of the scores.
 
 // Producer: each row's segments twice (pass 1, then pass 2), in order through the ring, with
 // the row's record {limit, batch entry, head, segment} beside every segment.  A row with no
@@ -1134,13 +1135,14 @@ const void *fwd_stream_fn(fos_dtype dt) {
 // ------------------------------------------------------ short rows: one warp per row
 //
 // A row of at most KT (<= 8) tiles is taken by one warp alone: it waits for the row's copy,
-// runs pass 1 on all its tiles (pairs of neighbouring tiles), folds the tile states with the
-// same merge, and writes P from the e_j it parked in tensor memory (its lane quarter w % 4,
-// warps sharing a quarter side by side in its columns).  No barrier joins the warps of a
-// CTA, so the merge of one row does not idle the others.  Each warp keeps its own ring of
-// a.stages row buffers and its lane 0 issues its own copies: the copy of row k + stages goes into
-// the buffer of row k as soon as pass 1 of row k has read it.  The per-tile arithmetic, the
-// merge and pass 2 are those of fos_fwd_kernel, so a row gives the same bits on either kernel.
+// runs pass 1 on all its tiles (pairs of neighbouring tiles), folds the tile states with
+// merge_tiles8 (merge_tiles' steps for at most 8 tiles), and writes P from the e_j it parked in
+// tensor memory (its lane quarter w % 4, warps sharing a quarter side by side in its columns).
+// No barrier joins the warps of a CTA, so the merge of one row does not idle the others.  Each
+// warp keeps its own ring of a.stages row buffers and its lane 0 issues its own copies: the copy
+// of row k + stages goes into the buffer of row k as soon as pass 1 of row k has read it.  The
+// per-tile arithmetic, the merge and pass 2 are those of fos_fwd_kernel, so a row gives the same
+// bits on either kernel.
 
 template <typename T, int KT>
 __global__ void __maxnreg__(KT == 2 ? 72 : 64) fos_fwd_rowwarp_kernel(const FwdArgs a) {
