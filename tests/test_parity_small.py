@@ -15,7 +15,10 @@ from gpu_util import (DTYPES, assert_check, bits_equal, check_bwd, check_fwd, de
 
 pytestmark = pytest.mark.gpu
 
-LENGTHS = [1, 7, 8, 255, 256, 257, 1000, 4352]
+# tiny rows, a lane's 8 keys, the tile (256), the one-warp kernel's 2 / 4 / 8-tile instances on
+# both sides of each boundary (512, 1024, 2048 keys; 2049 goes to the row groups), Qwen-Image's
+# 4352
+LENGTHS = [1, 2, 3, 7, 8, 255, 256, 257, 511, 512, 513, 1000, 1024, 1025, 2048, 2049, 4352]
 MASKS = ["none", "causal", "kvlen", "keymask", "sink", "all"]
 
 
